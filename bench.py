@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the attention forward on GB300: one JSON line on stdout (rank 0).
+
+A step is one vt_attn_fwd call over the whole workload (default: B=8, H=16,
+S_q=S_k=8192, D=128, bf16, causal, Q ~ N(0, 4^2), K, V ~ N(0, 1), seed 4).
+
+  value        TFLOP/s over the timed steps, inputs resident in HBM (flops = 4*B*H*S_q*S_k*D,
+               halved for causal; 2*B*H*S_q*S_k*(D_qk+D_v) in general), CUDA events on the
+               launching stream, max over ranks; inputs (805 MB) are larger than L2.
+  e2e          the same metric with the host->device copies of Q, K, V from pinned memory and
+               the device->host copy of O inside the timed region.
+  roofline     the kernel against the measured dense bf16 (or derived tf32) tensor peak.
+  cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload (rank 0 only).
+
+--impl reference times that oracle as the reference arm.  Under torchrun each rank
+runs its own copy of the workload on its own GPU (replicas, weak scaling; no
+collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 dense tensor peak"
+DEFAULT_WORKLOAD = "bf16_causal_8k_peaky"
+KERNEL_SOURCES = [os.path.join(ROOT, "scaled_dot_product_vt_gb300", "csrc", f)
+                  for f in ("vt_attn_kernel.cuh", "vt_ptx.cuh", "vt_attn_api.cu")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+# nominal dense tf32 : bf16 tensor ratio (1.1 : 2.25 PFLOP/s), applied to the measured bf16 peak
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+def load_traffic(workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_hash") != kernel_source_hash() or t.get("workload") != workload:
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_sample(w, q, k, v, causal: bool, target_s: float = 12.0, max_slices: int = 32):
+    """Time the fp64 oracle on whole (b, h) slices of the workload until ~target_s seconds have passed."""
+    import oracle
+    nthreads = oracle.default_threads()
+    rows_per_slice = w.S_q
+    done_flops, t_total, slices = 0.0, 0.0, 0
+    for s in range(max_slices):
+        b, h = divmod(s, w.H)
+        b %= w.B
+        rows = np.stack([np.full(rows_per_slice, b), np.full(rows_per_slice, h), np.arange(rows_per_slice)], axis=1)
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        done_flops += w.flops(causal) / (w.B * w.H)
+        slices += 1
+        if t_total >= target_s:
+            break
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{slices} whole (b,h) slice(s) of {w.name} ({w.S_q} rows each, causal={causal}), "
+                      f"{t_total:.1f} s fp64 on {nthreads} host threads"}
+
+
+def run_reference(args, w, causal):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = synth.make_workload(w)
+    import oracle
+    nthreads = oracle.default_threads()
+    slice_flops = w.flops(causal) / (w.B * w.H)
+    rows_per_step = max(1, min(w.S_q, int(args.ref_rows)))
+    # each step: the oracle over `rows_per_step` rows spread over one (b, h) slice
+    step_rows = np.linspace(0, w.S_q - 1, rows_per_step).astype(np.int64)
+    if causal:
+        step_flops = float(sum(2.0 * (i + 1) * (w.D_qk + w.D_v) for i in step_rows))
+    else:
+        step_flops = 2.0 * rows_per_step * w.S_k * (w.D_qk + w.D_v)
+    del slice_flops
+    times = []
+    for it in range(args.warmup + args.steps):
+        b, h = divmod(it % (w.B * w.H), w.H)
+        rows = np.stack([np.full(len(step_rows), b), np.full(len(step_rows), h), step_rows], axis=1)
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = step_flops * len(times) / total / 1e12
+    sample = (f"{rows_per_step} query rows evenly spread over one (b,h) slice of {w.name} per step "
+              f"(causal={causal}), fp64 on {nthreads} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "S_q": w.S_q, "S_k": w.S_k, "D_qk": w.D_qk,
+                   "D_v": w.D_v, "causal": causal, "io_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--causal", type=int, default=None, help="override the workload's mode (0/1)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=512, help="reference arm: query rows per step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    w = synth.WORKLOADS[args.workload]
+    causal = bool(w.causal[-1] if args.causal is None else args.causal)
+    if args.impl == "reference":
+        return run_reference(args, w, causal)
+
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import scaled_dot_product_vt_gb300 as vt
+    vt.load()
+    vt_dtype = vt.VT_BF16 if w.dtype == "bf16" else vt.VT_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    q, k, v = synth.make_workload(w)
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+        return t.view(tdt) if a.dtype == np.uint16 else t
+
+    hq, hk, hv = pinned(q), pinned(k), pinned(v)
+    Q, K, V = (t.to(dev) for t in (hq, hk, hv))
+    O = torch.empty((w.B, w.H, w.S_q, w.D_v), dtype=tdt, device=dev)
+    hO = torch.empty(O.shape, dtype=tdt).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flops = w.flops(causal)
+
+    def step():
+        rc = vt.vt_attn_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), w.B, w.H, w.S_q, w.S_k,
+                            w.D_qk, w.D_v, w.scale, int(causal), vt_dtype, sh)
+        if rc != 0:
+            raise RuntimeError(f"vt_attn_fwd: {vt.vt_status_str(rc)}")
+
+    for _ in range(args.warmup):
+        step()
+    st = vt.vt_last_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {vt.vt_status_str(st)}")
+
+    # ---- kernel-only timed region: inputs resident in HBM
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    st = vt.vt_last_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {vt.vt_status_str(st)}")
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(total_ms, world, dev)
+
+    # ---- end to end through the public API: pinned host -> device, kernel, device -> host
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e2e_ev[0].record(stream)
+    for _ in range(args.steps):
+        Q.copy_(hq, non_blocking=True)
+        K.copy_(hk, non_blocking=True)
+        V.copy_(hv, non_blocking=True)
+        step()
+        hO.copy_(O, non_blocking=True)
+    e2e_ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e2e_ev[0].elapsed_time(e2e_ev[1]), world, dev)
+    st = vt.vt_last_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status after e2e steps: {vt.vt_status_str(st)}")
+
+    peaks = load_peaks()
+    peak = peaks["bf16"] if w.dtype == "bf16" else peaks["bf16"] * TF32_OVER_BF16
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    per_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    in_bytes = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    out_bytes = hO.numel() * hO.element_size()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_oracle_sample(w, q, k, v, causal, target_s=args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S_q": w.S_q, "S_k": w.S_k, "D_qk": w.D_qk,
+                       "D_v": w.D_v, "causal": causal, "flops_per_step": flops,
+                       "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "peak_frac": value / world / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": load_traffic(w.name),
+                         "peak_source": (f"{peaks['source']} bf16 burst" if w.dtype == "bf16"
+                                         else f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio"),
+                         "kernel": f"vt::attn_fwd_kernel<{'1' if w.dtype == 'bf16' else '0'}>",
+                         "launch_ms": per_launch_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes},
+            "gpu_launches": args.steps,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+/*
+ * vt_attn — scaled dot-product attention forward on one GB300 GPU (sm_103a).
+ *
+ * The operation (VeriTile page "VeriTile.Examples.FlashAttention1.NaiveRefinement":
+ * fa1NaiveReference4D and fa1NaiveCausalReference4D, with the sequence-boundary and
+ * head-dimension-tail write contract of fa1_boundaryD_refines_naive_reference_views;
+ * separate query/key and value widths as in the accy page
+ * "tiny.accy.kernel.library.attention", spec fields `qk` and `value`):
+ *
+ *   for every batch b < B, head h < H, query row i < S_q and value column e < D_v
+ *     O[b,h,i,e] = sum_{j in A_i} softmax_j( scale * sum_{d<D_qk} Q[b,h,i,d] K[b,h,j,d] ) V[b,h,j,e]
+ *   where A_i = { j < S_k } (causal = 0) or { j < S_k : j <= i } (causal != 0; key j
+ *   <= query i counted from index 0 of both sequences).
+ *
+ * Layouts.  Q is [B,H,S_q,D_qk], K is [B,H,S_k,D_qk], V is [B,H,S_k,D_v] and O is
+ * [B,H,S_q,D_v], the last index contiguous (stride 1).  vt_attn_fwd takes the packed
+ * row-major layout; vt_attn_fwd_strided takes element strides for the (b, h, s)
+ * indices of each tensor.  All four pointers are DEVICE pointers (CUDA global memory
+ * of the current device).
+ *
+ * Element types.  VT_BF16: bf16 in, bf16 out, products accumulated in fp32 on the
+ * tensor cores (probabilities are rounded to bf16 before the P*V product).
+ * VT_F32: fp32 in, fp32 out, products on the TF32 tensor-core path with fp32
+ * accumulation (inputs and probabilities keep the TF32 subset of their bits).
+ *
+ * Ownership.  The caller owns every buffer.  The library allocates no device memory
+ * per call: tensor maps are built on the host and passed by value to the kernel.
+ *
+ * Writes.  Only O's logical elements (i < S_q, e < D_v of each (b, h)) are written;
+ * memory between rows or heads of a strided O is never touched.  O must not overlap
+ * Q, K or V.
+ *
+ * Asynchrony.  Calls enqueue work on `stream` and return without waiting.  A kernel
+ * that detects a problem on the device (a pipeline wait that exceeds its time limit)
+ * records it in a device status word instead of faulting; vt_last_device_status
+ * synchronises the stream and returns (and clears) that status.  If the environment
+ * variable VT_CHECK is set to a non-zero value, every call does this itself.
+ *
+ * Argument errors are detected on the host before anything is launched:
+ *   VT_ERR_INVALID_ARG   a NULL pointer, a negative extent, S_k, D_qk or D_v equal to 0,
+ *                        an unknown dtype, a non-finite scale, O overlapping Q/K/V,
+ *                        or a non-positive stride;
+ *   VT_ERR_UNSUPPORTED   D_qk or D_v above 128, or an extent beyond 2^31 - 1;
+ *   VT_ERR_MISALIGNED    a pointer not 16-byte aligned, or a (b, h, s) stride whose
+ *                        byte size is not a multiple of 16 (the TMA engine's rule);
+ *   VT_ERR_CUDA          a CUDA runtime or driver call failed (no device, launch error).
+ * B, H or S_q equal to 0 is a valid empty problem: VT_OK, nothing launched.
+ */
+#ifndef VT_ATTN_H
+#define VT_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *vt_stream_t;
+
+typedef enum { VT_F32 = 0, VT_BF16 = 1 } vt_dtype;
+
+typedef enum {
+    VT_OK = 0,
+    VT_ERR_INVALID_ARG = 1,
+    VT_ERR_UNSUPPORTED = 2,
+    VT_ERR_MISALIGNED = 3,
+    VT_ERR_CUDA = 4,
+    VT_ERR_DEVICE_TIMEOUT = 5,
+    VT_ERR_DEVICE_BOUNDS = 6
+} vt_status;
+
+/*
+ * Attention forward on packed [B,H,S,D] tensors (the operation above).
+ * Q, K, V: device pointers to the inputs (read only).  O: device pointer to the output.
+ * scale: the factor applied to every dot product (the VeriTile reference's `scale`
+ * parameter; 1/sqrt(D_qk) is the usual choice).  causal: 0 or non-zero.
+ */
+vt_status vt_attn_fwd(const void *Q, const void *K, const void *V, void *O,
+                      int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                      int64_t D_qk, int64_t D_v,
+                      float scale, int causal, vt_dtype dtype, vt_stream_t stream);
+
+/*
+ * The same operation on strided tensors.  x_stride[0..2] are the element strides of
+ * the b, h and s indices of tensor x; its last index has stride 1.  Every stride must
+ * be positive and its byte size a multiple of 16.
+ */
+vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3],
+                              const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3],
+                              void *O, const int64_t o_stride[3],
+                              int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                              int64_t D_qk, int64_t D_v,
+                              float scale, int causal, vt_dtype dtype, vt_stream_t stream);
+
+/*
+ * Options for vt_attn_fwd_ex.  A zeroed struct gives the defaults of vt_attn_fwd.
+ *   wait_timeout_ns  limit for any single pipeline wait inside the kernel before it
+ *                    gives up, records VT_ERR_DEVICE_TIMEOUT and exits cleanly
+ *                    (0: 2 seconds).
+ *   flags            VT_OPT_TEST_STALL makes the kernel wait on a barrier that is never
+ *                    signalled, so that the time-limit path can be tested; it does no
+ *                    attention work and leaves O unwritten.
+ */
+#define VT_OPT_TEST_STALL 1u
+typedef struct {
+    uint64_t wait_timeout_ns;
+    uint32_t flags;
+    uint32_t reserved;
+} vt_attn_opts;
+
+/* vt_attn_fwd_strided with options (opts may be NULL). */
+vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3],
+                         const void *K, const int64_t k_stride[3],
+                         const void *V, const int64_t v_stride[3],
+                         void *O, const int64_t o_stride[3],
+                         int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                         int64_t D_qk, int64_t D_v,
+                         float scale, int causal, vt_dtype dtype,
+                         const vt_attn_opts *opts, vt_stream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char *vt_status_str(vt_status status);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word of the current
+ * device: VT_OK, VT_ERR_DEVICE_TIMEOUT or VT_ERR_DEVICE_BOUNDS; VT_ERR_CUDA if the
+ * synchronisation itself reports an error.
+ */
+vt_status vt_last_device_status(vt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VT_ATTN_H */

@@ -1,0 +1,225 @@
+// Host side of the vt_attn C ABI: argument checks, TMA tensor maps, launch.
+//
+// The operation and its argument contract are stated in include/vt_attn.h.  Nothing here
+// touches the GPU before every argument has been checked.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/vt_attn.h"
+#include "vt_attn_kernel.cuh"
+
+namespace vt {
+
+__device__ unsigned g_status_word;  // device status bits (kStatusTimeout, kStatusBounds)
+
+namespace {
+
+constexpr int64_t kMaxD = 128;
+constexpr int64_t kMaxExtent = 0x7FFFFFFF;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr int kSmemLimit = 232448;  // 227 KiB per CTA on sm_100-class parts
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi) bytes touched by a tensor's logical elements
+};
+
+Span span_of(const void *p, const int64_t st[3], int64_t B, int64_t H, int64_t S, int64_t D, int elt) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    const int64_t last = (B - 1) * st[0] + (H - 1) * st[1] + (S - 1) * st[2] + (D - 1);
+    return {lo, lo + static_cast<uintptr_t>(last + 1) * elt};
+}
+
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool env_check() {
+    static const bool on = [] {
+        const char *v = std::getenv("VT_CHECK");
+        return v && v[0] && !(v[0] == '0' && v[1] == 0);
+    }();
+    return on;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D map over [B][H][S][D] (D innermost), box = 128-byte chunk of D x `rows` rows of S.
+bool make_map(CUtensorMap *map, const void *ptr, const int64_t st[3], int64_t B, int64_t H, int64_t S, int64_t D,
+              int elt, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2] * elt), static_cast<cuuint64_t>(st[1] * elt),
+                                   static_cast<cuuint64_t>(st[0] * elt)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(rows), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int DT>
+vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
+                 const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                 int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, cudaStream_t stream) {
+    using C = Cfg<DT>;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, C::kBN) ||
+        !make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, C::kBN))
+        return VT_ERR_CUDA;
+
+    AttnParams p{};
+    p.B = static_cast<int>(B);
+    p.H = static_cast<int>(H);
+    p.S_q = static_cast<int>(S_q);
+    p.S_k = static_cast<int>(S_k);
+    p.D_qk = static_cast<int>(D_qk);
+    p.D_v = static_cast<int>(D_v);
+    p.n_qblocks = static_cast<int>((S_q + kBM - 1) / kBM);
+    p.qk_ksteps = static_cast<int>((D_qk + C::kKStep - 1) / C::kKStep);
+    p.q_chunks = static_cast<int>((D_qk + C::kChunkElems - 1) / C::kChunkElems);
+    p.v_chunks = static_cast<int>((D_v + C::kChunkElems - 1) / C::kChunkElems);
+    p.n_pv = static_cast<int>((D_v + 15) / 16 * 16);
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.O = O;
+    p.o_sb = os[0];
+    p.o_sh = os[1];
+    p.o_ss = os[2];
+    p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
+    p.flags = opts ? opts->flags : 0u;
+
+    const int q_bytes = p.q_chunks * kBM * 128;
+    const int kv_bytes = (p.q_chunks + p.v_chunks) * C::kBN * 128;
+    const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
+    p.stages = (budget - q_bytes) / kv_bytes;
+    if (p.stages > kMaxStages) p.stages = kMaxStages;
+    if (p.stages < 2) return VT_ERR_UNSUPPORTED;
+    const int smem = 1024 + q_bytes + p.stages * kv_bytes;
+
+    void *status_ptr = nullptr;
+    if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return VT_ERR_CUDA;
+    p.status = static_cast<unsigned *>(status_ptr);
+
+    auto kern = attn_fwd_kernel<DT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return VT_ERR_CUDA;
+    const long long items = static_cast<long long>(p.n_qblocks) * B * H;
+    if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+    kern<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+    return VT_OK;
+}
+
+vt_status read_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return VT_ERR_CUDA;
+    unsigned w = 0;
+    if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof w) != cudaSuccess) return VT_ERR_CUDA;
+    if (w) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return VT_ERR_CUDA;
+    }
+    if (w & kStatusTimeout) return VT_ERR_DEVICE_TIMEOUT;
+    if (w & kStatusBounds) return VT_ERR_DEVICE_BOUNDS;
+    return VT_OK;
+}
+
+}  // namespace
+}  // namespace vt
+
+extern "C" {
+
+const char *vt_status_str(vt_status s) {
+    switch (s) {
+        case VT_OK: return "VT_OK";
+        case VT_ERR_INVALID_ARG: return "VT_ERR_INVALID_ARG: invalid argument";
+        case VT_ERR_UNSUPPORTED: return "VT_ERR_UNSUPPORTED: shape not supported (D_qk, D_v <= 128; extents < 2^31)";
+        case VT_ERR_MISALIGNED: return "VT_ERR_MISALIGNED: pointers must be 16-byte aligned and strides 16-byte multiples";
+        case VT_ERR_CUDA: return "VT_ERR_CUDA: a CUDA runtime or driver call failed";
+        case VT_ERR_DEVICE_TIMEOUT: return "VT_ERR_DEVICE_TIMEOUT: a kernel pipeline wait exceeded its time limit";
+        case VT_ERR_DEVICE_BOUNDS: return "VT_ERR_DEVICE_BOUNDS: a kernel index check failed";
+    }
+    return "unknown vt_status";
+}
+
+vt_status vt_last_device_status(vt_stream_t stream) { return vt::read_status(reinterpret_cast<cudaStream_t>(stream)); }
+
+vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                         const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
+                         int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
+                         vt_dtype dtype, const vt_attn_opts *opts, vt_stream_t stream) {
+    if (dtype != VT_F32 && dtype != VT_BF16) return VT_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || S_q < 0 || S_k < 0 || D_qk < 0 || D_v < 0) return VT_ERR_INVALID_ARG;
+    if (S_k == 0 || D_qk == 0 || D_v == 0) return VT_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return VT_ERR_INVALID_ARG;
+    if (D_qk > vt::kMaxD || D_v > vt::kMaxD) return VT_ERR_UNSUPPORTED;
+    if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxExtent || S_k > vt::kMaxExtent)
+        return VT_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || S_q == 0) return VT_OK;
+    if (!Q || !K || !V || !O || !q_stride || !k_stride || !v_stride || !o_stride) return VT_ERR_INVALID_ARG;
+    const int elt = dtype == VT_BF16 ? 2 : 4;
+    const int64_t *st[4] = {q_stride, k_stride, v_stride, o_stride};
+    for (const int64_t *s : st)
+        for (int i = 0; i < 3; ++i)
+            if (s[i] <= 0) return VT_ERR_INVALID_ARG;
+    const void *ptrs[4] = {Q, K, V, O};
+    for (const void *ptr : ptrs)
+        if (reinterpret_cast<uintptr_t>(ptr) % 16) return VT_ERR_MISALIGNED;
+    for (const int64_t *s : st)
+        for (int i = 0; i < 3; ++i)
+            if ((s[i] * elt) % 16) return VT_ERR_MISALIGNED;
+    const vt::Span so = vt::span_of(O, o_stride, B, H, S_q, D_v, elt);
+    if (vt::overlap(so, vt::span_of(Q, q_stride, B, H, S_q, D_qk, elt)) ||
+        vt::overlap(so, vt::span_of(K, k_stride, B, H, S_k, D_qk, elt)) ||
+        vt::overlap(so, vt::span_of(V, v_stride, B, H, S_k, D_v, elt)))
+        return VT_ERR_INVALID_ARG;
+
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const vt_status r = dtype == VT_BF16
+                            ? vt::launch<vt::kBF16>(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k,
+                                                    D_qk, D_v, scale, causal, opts, s)
+                            : vt::launch<vt::kF32>(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k,
+                                                   D_qk, D_v, scale, causal, opts, s);
+    if (r != VT_OK) return r;
+    return vt::env_check() ? vt::read_status(s) : VT_OK;
+}
+
+vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
+                              int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
+                              vt_dtype dtype, vt_stream_t stream) {
+    return vt_attn_fwd_ex(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale,
+                          causal, dtype, nullptr, stream);
+}
+
+vt_status vt_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t B, int64_t H, int64_t S_q,
+                      int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype,
+                      vt_stream_t stream) {
+    const int64_t qs[3] = {H * S_q * D_qk, S_q * D_qk, D_qk};
+    const int64_t ks[3] = {H * S_k * D_qk, S_k * D_qk, D_qk};
+    const int64_t vs[3] = {H * S_k * D_v, S_k * D_v, D_v};
+    const int64_t os[3] = {H * S_q * D_v, S_q * D_v, D_v};
+    return vt_attn_fwd_ex(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, dtype, nullptr,
+                          stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,420 @@
+// Attention forward kernel for sm_103a: O = softmax(scale * Q K^T) V per (batch, head).
+//
+// One CTA computes one work item: a 128-row query block of one (b, h) slice.  Warp roles:
+//   warp 0      TMA producer: the Q block once, then K and V tiles of BN keys through a
+//               `stages`-deep ring of shared-memory slots (mbarrier full/empty pairs).
+//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a TMEM score
+//               buffer (two buffers, alternating), then O += P_j V_j with P_j read from TMEM.
+//   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
+//               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
+//               over S_j, O rescale when the reference max moves, and the epilogue.
+//
+// The tiling follows the FA-1 boundary kernel of the VeriTile page
+// "VeriTile.Examples.FlashAttention1.NaiveRefinement" (M query rows per program, key
+// blocks of Bk, a head tile of Bd >= D, writes only where row < S_q and d < D); the four
+// reductions are the accy page's score_dot, score_max, score_exp_sum and
+// value_weighted_sum, computed online; the exp2-with-folded-scale form is the "Base-2
+// scaled attention" of the VeriTile coverage table (sm_scale * log2(e)).
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "vt_ptx.cuh"
+
+namespace vt {
+
+constexpr int kBM = 128;           // query rows per work item (= TMEM lanes)
+constexpr int kMaxStages = 4;
+constexpr int kThreads = 192;      // 6 warps
+constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
+
+// Device status bits (the host maps them to vt_status codes).
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBounds = 2u;
+
+enum : int { kF32 = 0, kBF16 = 1 };
+
+struct AttnParams {
+    int B, H, S_q, S_k, D_qk, D_v;
+    int n_qblocks;    // ceil(S_q / 128)
+    int qk_ksteps;    // ceil(D_qk / K-step), K-step = 16 (bf16) or 8 (tf32)
+    int q_chunks;     // 128-byte column chunks of a Q/K row: ceil(D_qk * elt / 128)
+    int v_chunks;     // 128-byte column chunks of a V row
+    int n_pv;         // MMA N of P*V: D_v rounded up to 16
+    int stages;
+    int causal;
+    float scale_log2;  // scale * log2(e)
+    void *O;
+    long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
+    unsigned long long timeout_ns;
+    unsigned flags;
+    unsigned *status;  // device status word
+};
+
+template <int DT>
+struct Cfg {
+    static constexpr int kElt = DT == kBF16 ? 2 : 4;
+    static constexpr int kBN = DT == kBF16 ? 128 : 64;         // keys per tile
+    static constexpr int kKStep = DT == kBF16 ? 16 : 8;        // MMA K per instruction
+    static constexpr int kChunkElems = 128 / kElt;             // elements per 128-byte chunk
+    static constexpr uint32_t kFmt = DT == kBF16 ? 1u : 2u;    // bf16 / tf32
+    static constexpr uint32_t kTmemCols = DT == kBF16 ? 512u : 256u;
+    static constexpr uint32_t kColS0 = 0, kColS1 = kBN, kColO = 2 * kBN;
+};
+
+struct SharedCtl {
+    uint64_t full_k[kMaxStages];
+    uint64_t full_v[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done;
+    uint64_t drain;
+    uint64_t stall;
+    uint32_t tmem_base;
+    volatile uint32_t abort_flag;
+};
+
+// Wait for the phase of `bar` with `parity`, giving up after the time limit or when
+// another role has aborted.  Returns false on give-up (after flagging the abort).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl &ctl, const AttnParams &p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (ctl.abort_flag) return false;
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                ctl.abort_flag = 1;
+                atomicOr(p.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait without the abort shortcut (used while draining copies in flight on the abort path).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const AttnParams &p) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using C = Cfg<DT>;
+    constexpr int BN = C::kBN;
+    __shared__ SharedCtl ctl;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Work item: all heads' heaviest causal query blocks first.
+    const int bh_count = p.B * p.H;
+    const int slot = blockIdx.x / bh_count;
+    const int bh = blockIdx.x - slot * bh_count;
+    const int qb = p.causal ? (p.n_qblocks - 1 - slot) : slot;
+    const int h = bh % p.H;
+    const int b = bh / p.H;
+    const int q_row0 = qb * kBM;
+    const int n_ktiles_all = (p.S_k + BN - 1) / BN;
+    int n_kv = n_ktiles_all;
+    if (p.causal) {
+        const int last_row = min(q_row0 + kBM, p.S_q) - 1;
+        n_kv = min(n_kv, last_row / BN + 1);
+    }
+
+    // Shared-memory carve-up (1024-byte aligned for the 128-byte swizzle).
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t q_bytes = p.q_chunks * kBM * 128;
+    const uint32_t k_bytes = p.q_chunks * BN * 128;
+    const uint32_t v_bytes = p.v_chunks * BN * 128;
+    const uint32_t sQ = base;
+    auto sK = [&](int st) { return base + q_bytes + st * (k_bytes + v_bytes); };
+    auto sV = [&](int st) { return base + q_bytes + st * (k_bytes + v_bytes) + k_bytes; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&ctl.full_k[s]), 1);
+            mbar_init(smem_u32(&ctl.full_v[s]), 1);
+            mbar_init(smem_u32(&ctl.empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl.q_full), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&ctl.s_full[i]), 1);
+            mbar_init(smem_u32(&ctl.p_full[i]), 128);
+        }
+        mbar_init(smem_u32(&ctl.o_done), 1);
+        mbar_init(smem_u32(&ctl.drain), 1);
+        mbar_init(smem_u32(&ctl.stall), 1);
+        ctl.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl.tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_bytes);
+            for (int c = 0; c < p.q_chunks; ++c)
+                tma_load_4d(sQ + c * kBM * 128, &tmQ, smem_u32(&ctl.q_full), c * C::kChunkElems, q_row0, h, b);
+            int issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int st = j % p.stages;
+                const int use = j / p.stages;
+                if (use > 0 && !wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl, p)) break;
+                mbar_arrive_expect_tx(smem_u32(&ctl.full_k[st]), k_bytes);
+                for (int c = 0; c < p.q_chunks; ++c)
+                    tma_load_4d(sK(st) + c * BN * 128, &tmK, smem_u32(&ctl.full_k[st]), c * C::kChunkElems, j * BN,
+                                h, b);
+                mbar_arrive_expect_tx(smem_u32(&ctl.full_v[st]), v_bytes);
+                for (int c = 0; c < p.v_chunks; ++c)
+                    tma_load_4d(sV(st) + c * BN * 128, &tmV, smem_u32(&ctl.full_v[st]), c * C::kChunkElems, j * BN,
+                                h, b);
+                issued = j + 1;
+            }
+            if (ctl.abort_flag) {
+                // Let every copy this thread started land before the CTA's memory goes away.
+                wait_drain(smem_u32(&ctl.q_full), 0, p);
+                for (int j = max(0, issued - p.stages); j < issued; ++j) {
+                    const int st = j % p.stages;
+                    wait_drain(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, p);
+                    wait_drain(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, p);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
+            const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, 1);
+            bool ok = true, any_mma = false;
+            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl, p);  // test hook: never signalled
+            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl, p);
+            tc_fence_after();
+
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j % p.stages;
+                if (!wait_bounded(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, ctl, p)) return false;
+                tc_fence_after();
+                const uint32_t d = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
+                for (int kk = 0; kk < p.qk_ksteps; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kBM * 128 + off, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
+                    if (DT == kBF16) mma_ss(d, a, bd, idesc_qk, kk > 0);
+                    else mma_ss_tf32(d, a, bd, idesc_qk, kk > 0);
+                }
+                mma_commit(smem_u32(&ctl.s_full[j & 1]));
+                any_mma = true;
+                return true;
+            };
+
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
+                const int st = j % p.stages;
+                if (!wait_bounded(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, ctl, p)) { ok = false; break; }
+                if (!wait_bounded(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, ctl, p)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_base = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
+                for (int kk = 0; kk < BN / C::kKStep; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(sV(st) + kk * C::kKStep * 128, BN * 128, 1024);
+                    if (DT == kBF16) mma_ts(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
+                    else mma_ts_tf32(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
+                }
+                mma_commit(smem_u32(&ctl.empty[st]));
+                mma_commit(smem_u32(&ctl.o_done));
+            }
+            if (!ok && any_mma) {
+                mma_commit(smem_u32(&ctl.drain));
+                wait_drain(smem_u32(&ctl.drain), 0, p);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;          // row of the query block owned by this thread
+        const int q_row = q_row0 + row;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const float c = p.scale_log2;
+        float m_used = -INFINITY;  // reference max (log2 units) of O and l
+        float l = 0.0f;
+        bool ok = true;
+
+        for (int j = 0; j < n_kv; ++j) {
+            ok = wait_bounded(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, ctl, p);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::kColS1 : C::kColS0);
+            uint32_t sr[BN];
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+            tmem_wait_ld();
+
+            float x[BN];
+#pragma unroll
+            for (int k = 0; k < BN; ++k) x[k] = __uint_as_float(sr[k]) * c;
+            const int k0 = j * BN;
+            const bool need_mask = (k0 + BN > p.S_k) || (p.causal && k0 + BN - 1 > q_row0);
+            if (need_mask) {
+                const int lim = p.causal ? min(p.S_k, q_row + 1) : p.S_k;  // keys k0+k < lim are allowed
+#pragma unroll
+                for (int k = 0; k < BN; ++k)
+                    if (k0 + k >= lim) x[k] = -INFINITY;
+            }
+            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+            for (int k = 4; k < BN; k += 4) {
+                mx0 = fmaxf(mx0, x[k]);
+                mx1 = fmaxf(mx1, x[k + 1]);
+                mx2 = fmaxf(mx2, x[k + 2]);
+                mx3 = fmaxf(mx3, x[k + 3]);
+            }
+            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const float m_new = fmaxf(m_used, m_tile);
+            // Lazy rescale: keep the old reference unless the max grew by more than tau.
+            const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kRescaleTau);
+            float alpha = 1.0f;
+            if (resc) {
+                alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);
+                l *= alpha;
+                m_used = m_new;
+            }
+            const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+            for (int k = 0; k < BN; k += 4) {
+                x[k] = ex2(x[k] - m_ref);
+                x[k + 1] = ex2(x[k + 1] - m_ref);
+                x[k + 2] = ex2(x[k + 2] - m_ref);
+                x[k + 3] = ex2(x[k + 3] - m_ref);
+                l0 += x[k];
+                l1 += x[k + 1];
+                l2 += x[k + 2];
+                l3 += x[k + 3];
+            }
+            l += (l0 + l1) + (l2 + l3);
+
+            // P_j over S_j in TMEM: bf16 pairs packed two per column, or fp32 one per column.
+            if (DT == kBF16) {
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int k = 0; k < BN / 2; ++k) pk[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+                for (int cc = 0; cc < BN / 64; ++cc) tmem_st32(s_addr + cc * 32, pk + cc * 32);
+            } else {
+                uint32_t pk[BN];
+#pragma unroll
+                for (int k = 0; k < BN; ++k) pk[k] = __float_as_uint(x[k]);
+#pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc) tmem_st32(s_addr + cc * 32, pk + cc * 32);
+            }
+
+            // O *= alpha for rows whose reference moved, once P_{j-1} V_{j-1} has landed.
+            if (j > 0) {
+                ok = wait_bounded(smem_u32(&ctl.o_done), (j - 1) & 1, ctl, p);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, resc)) {
+                    const uint32_t o_addr = tmem + lane_base + C::kColO;
+                    for (int cc = 0; cc < p.n_pv; cc += 16) {
+                        uint32_t o[16];
+                        tmem_ld16(o_addr + cc, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st16(o_addr + cc, o);
+                    }
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
+        }
+
+        if (ok) {
+            ok = wait_bounded(smem_u32(&ctl.o_done), (n_kv - 1) & 1, ctl, p);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            // ------------------------------------------------------------ epilogue
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+            const uint32_t o_addr = tmem + lane_base + C::kColO;
+            const bool row_ok = q_row < p.S_q;
+            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                            (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
+                             static_cast<long long>(q_row) * p.o_ss) * C::kElt;
+            for (int cc = 0; cc < p.n_pv; cc += 16) {
+                uint32_t o[16];
+                tmem_ld16(o_addr + cc, o);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(o[k]) * inv_l;
+                if (DT == kBF16) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+                    if (cc + 16 <= p.D_v) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                    }
+                } else {
+                    if (cc + 16 <= p.D_v) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + cc * 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    } else {
+                        float *dst = reinterpret_cast<float *>(orow) + cc;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) dst[k] = v[k];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace vt

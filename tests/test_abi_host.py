@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header declares, and
+rejects bad arguments before launching anything (these run without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import scaled_dot_product_vt_gb300 as vt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vt_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    vt.build()
+    return vt.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vt_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(vt.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in vt.STATUS.items():
+        assert vt.vt_status_str(code).startswith(name)
+    assert vt.vt_status_str(99) == "unknown vt_status"
+
+
+A = 1 << 20  # fake, 16-byte aligned, distinct "device" addresses: never dereferenced on these paths
+
+
+def call(B=1, H=1, S_q=4, S_k=4, D_qk=8, D_v=8, scale=0.5, causal=0, dtype=vt.VT_BF16,
+         ptrs=(A, 2 * A, 3 * A, 4 * A)):
+    return vt.vt_attn_fwd(*ptrs, B, H, S_q, S_k, D_qk, D_v, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S_k=0), 1), (dict(D_qk=0), 1), (dict(D_v=0), 1),
+    (dict(B=-1), 1), (dict(H=-2), 1), (dict(S_q=-1), 1), (dict(S_k=-5), 1),
+    (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(D_qk=129), 2), (dict(D_v=256), 2), (dict(S_q=1 << 31), 2),
+    (dict(ptrs=(A, 2 * A, 3 * A, 0)), 1), (dict(ptrs=(0, 2 * A, 3 * A, 4 * A)), 1),
+    (dict(ptrs=(A + 8, 2 * A, 3 * A, 4 * A)), 3), (dict(ptrs=(A, 2 * A, 3 * A, 4 * A + 2)), 3),
+    (dict(D_qk=4, dtype=vt.VT_BF16), 3),        # row pitch 8 bytes: not a TMA stride
+    (dict(D_v=20, dtype=vt.VT_BF16), 3),        # 40-byte rows
+    (dict(ptrs=(A, 2 * A, 3 * A, A + 32)), 1),  # O overlaps Q
+])
+def test_argument_errors(lib, kw, code):
+    assert call(**kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(S_q=0), dict(B=0, ptrs=(0, 0, 0, 0))])
+def test_empty_problems_are_ok_without_launch(lib, kw):
+    assert call(**kw) == 0
+
+
+def test_strided_errors(lib):
+    good = (32, 32, 8)
+    assert vt.vt_attn_fwd_strided(A, good, 2 * A, good, 3 * A, good, 4 * A, (32, 32, 0),
+                                  1, 1, 4, 4, 8, 8, 0.5, 0, vt.VT_BF16, None) == 1
+    assert vt.vt_attn_fwd_strided(A, good, 2 * A, good, 3 * A, (32, 32, 12), 4 * A, good,
+                                  1, 1, 4, 4, 8, 8, 0.5, 0, vt.VT_BF16, None) == 3
+    # strided O whose rows interleave with V's span
+    assert vt.vt_attn_fwd_strided(A, good, 2 * A, good, 3 * A, good, 3 * A + 16, (64, 64, 16),
+                                  1, 1, 4, 4, 8, 8, 0.5, 0, vt.VT_BF16, None) == 1
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert call() == 4
+    assert vt.vt_last_device_status(0) == 4
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        vt.load(str(tmp_path / "libvt_attn.so"))
