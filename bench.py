@@ -20,6 +20,7 @@ collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -227,6 +228,7 @@ def main() -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--causal", type=int, default=None, help="override the workload's mode (0/1)")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's B (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=512, help="reference arm: query rows per step")
@@ -235,6 +237,8 @@ def main() -> int:
         ap.error("at least 3 warm-up steps")
 
     w = synth.WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_B{args.batch}")
     causal = bool(w.causal[-1] if args.causal is None else args.causal)
     if args.impl == "reference":
         return run_reference(args, w, causal)

@@ -83,9 +83,13 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
                  int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, cudaStream_t stream) {
     using C = Cfg<DT>;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, C::kBN) ||
-        !make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, C::kBN))
+    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, C::kBN))
         return VT_ERR_CUDA;
+    if (DT == kBF16) {
+        if (!make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, C::kBN)) return VT_ERR_CUDA;
+    } else {
+        tv = tk;  // fp32: V is read by the kernel's transposing loader warps, not by TMA
+    }
 
     AttnParams p{};
     p.B = static_cast<int>(B);
@@ -105,11 +109,15 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     p.o_sb = os[0];
     p.o_sh = os[1];
     p.o_ss = os[2];
+    p.V = V;
+    p.v_sb = vs[0];
+    p.v_sh = vs[1];
+    p.v_ss = vs[2];
     p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     p.flags = opts ? opts->flags : 0u;
 
     const int q_bytes = p.q_chunks * kBM * 128;
-    const int kv_bytes = (p.q_chunks + p.v_chunks) * C::kBN * 128;
+    const int kv_bytes = p.q_chunks * C::kBN * 128 + v_stage_bytes<DT>(p.v_chunks, p.n_pv);
     const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
     p.stages = (budget - q_bytes) / kv_bytes;
     if (p.stages > kMaxStages) p.stages = kMaxStages;
@@ -125,7 +133,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
         return VT_ERR_CUDA;
     const long long items = static_cast<long long>(p.n_qblocks) * B * H;
     if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
-    kern<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(tq, tk, tv, p);
+    kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
     return VT_OK;
 }

@@ -8,6 +8,10 @@
 //   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
 //               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
 //               over S_j, O rescale when the reference max moves, and the epilogue.
+//   warps 6-7   fp32 I/O only: V loader.  The TF32 MMA takes its B operand K-major only (an
+//               N-major tf32 B reads as zeros), so V tiles are read with coalesced 16-byte
+//               loads and written transposed (keys contiguous) into the 128-byte-swizzled
+//               K-major layout; for bf16, V goes by TMA as it is (N-major B).
 //
 // The tiling follows the FA-1 boundary kernel of the VeriTile page
 // "VeriTile.Examples.FlashAttention1.NaiveRefinement" (M query rows per program, key
@@ -26,7 +30,6 @@ namespace vt {
 
 constexpr int kBM = 128;           // query rows per work item (= TMEM lanes)
 constexpr int kMaxStages = 4;
-constexpr int kThreads = 192;      // 6 warps
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
 
 // Device status bits (the host maps them to vt_status codes).
@@ -47,6 +50,8 @@ struct AttnParams {
     float scale_log2;  // scale * log2(e)
     void *O;
     long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
+    const void *V;               // read by the fp32 V loader
+    long long v_sb, v_sh, v_ss;
     unsigned long long timeout_ns;
     unsigned flags;
     unsigned *status;  // device status word
@@ -61,7 +66,22 @@ struct Cfg {
     static constexpr uint32_t kFmt = DT == kBF16 ? 1u : 2u;    // bf16 / tf32
     static constexpr uint32_t kTmemCols = DT == kBF16 ? 512u : 256u;
     static constexpr uint32_t kColS0 = 0, kColS1 = kBN, kColO = 2 * kBN;
+    static constexpr int kThreads = DT == kBF16 ? 192 : 256;
+    static constexpr int kVLoaders = DT == kBF16 ? 0 : 64;
 };
+
+// Bytes of one V stage: bf16 keeps V N-major (128-byte column chunks of BN key rows); fp32
+// stores V^T K-major (n_pv rows of BN keys, in 128-byte key chunks).
+template <int DT>
+__host__ __device__ inline int v_stage_bytes(int v_chunks, int n_pv) {
+    return DT == kBF16 ? v_chunks * Cfg<DT>::kBN * 128 : n_pv * Cfg<DT>::kBN * 4;
+}
+
+// Byte offset of (row r, byte c) in a 1024-byte-aligned region of 128-byte rows laid out
+// the way the 128-byte TMA swizzle lays them out: 16-byte unit index XOR (row mod 8).
+__device__ __forceinline__ uint32_t swizzle128(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((((c >> 4) ^ (r & 7))) << 4) + (c & 15));
+}
 
 struct SharedCtl {
     uint64_t full_k[kMaxStages];
@@ -107,7 +127,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using C = Cfg<DT>;
@@ -138,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t q_bytes = p.q_chunks * kBM * 128;
     const uint32_t k_bytes = p.q_chunks * BN * 128;
-    const uint32_t v_bytes = p.v_chunks * BN * 128;
+    const uint32_t v_bytes = v_stage_bytes<DT>(p.v_chunks, p.n_pv);
     const uint32_t sQ = base;
     auto sK = [&](int st) { return base + q_bytes + st * (k_bytes + v_bytes); };
     auto sV = [&](int st) { return base + q_bytes + st * (k_bytes + v_bytes) + k_bytes; };
@@ -146,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&ctl.full_k[s]), 1);
-            mbar_init(smem_u32(&ctl.full_v[s]), 1);
+            mbar_init(smem_u32(&ctl.full_v[s]), DT == kBF16 ? 1 : C::kVLoaders);
             mbar_init(smem_u32(&ctl.empty[s]), 1);
         }
         mbar_init(smem_u32(&ctl.q_full), 1);
@@ -189,10 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < p.q_chunks; ++c)
                     tma_load_4d(sK(st) + c * BN * 128, &tmK, smem_u32(&ctl.full_k[st]), c * C::kChunkElems, j * BN,
                                 h, b);
-                mbar_arrive_expect_tx(smem_u32(&ctl.full_v[st]), v_bytes);
-                for (int c = 0; c < p.v_chunks; ++c)
-                    tma_load_4d(sV(st) + c * BN * 128, &tmV, smem_u32(&ctl.full_v[st]), c * C::kChunkElems, j * BN,
-                                h, b);
+                if (DT == kBF16) {
+                    mbar_arrive_expect_tx(smem_u32(&ctl.full_v[st]), v_bytes);
+                    for (int c = 0; c < p.v_chunks; ++c)
+                        tma_load_4d(sV(st) + c * BN * 128, &tmV, smem_u32(&ctl.full_v[st]), c * C::kChunkElems,
+                                    j * BN, h, b);
+                }
                 issued = j + 1;
             }
             if (ctl.abort_flag) {
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = max(0, issued - p.stages); j < issued; ++j) {
                     const int st = j % p.stages;
                     wait_drain(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, p);
-                    wait_drain(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, p);
+                    if (DT == kBF16) wait_drain(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, p);
                 }
             }
         }
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
-            const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, 1);
+            const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, DT == kBF16 ? 1 : 0);
             bool ok = true, any_mma = false;
             if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl, p);  // test hook: never signalled
             if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl, p);
@@ -241,9 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t a_base = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
                 for (int kk = 0; kk < BN / C::kKStep; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(sV(st) + kk * C::kKStep * 128, BN * 128, 1024);
-                    if (DT == kBF16) mma_ts(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
-                    else mma_ts_tf32(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
+                    if (DT == kBF16) {
+                        // V N-major: K-step = 16 key rows of 128 bytes; N chunks BN*128 bytes apart
+                        const uint64_t bd = smem_desc_sw128(sV(st) + kk * C::kKStep * 128, BN * 128, 1024);
+                        mma_ts(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
+                    } else {
+                        // V^T K-major: K-step = 8 keys = 32 bytes inside a 128-byte key chunk
+                        const uint64_t bd =
+                            smem_desc_sw128(sV(st) + (kk >> 2) * p.n_pv * 128 + (kk & 3) * 32, 16, 1024);
+                        mma_ts_tf32(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
+                    }
                 }
                 mma_commit(smem_u32(&ctl.empty[st]));
                 mma_commit(smem_u32(&ctl.o_done));
@@ -252,6 +281,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&ctl.drain));
                 wait_drain(smem_u32(&ctl.drain), 0, p);
             }
+        }
+    } else if (DT == kF32 && warp >= 6) {
+        // ------------------------------------------------------------ fp32 V loader (transposing)
+        const int lt = threadIdx.x - 192;
+        const int nd4 = p.n_pv / 4;  // 4-column groups, including the zero padding up to n_pv
+        const float *vbh = static_cast<const float *>(p.V) + static_cast<long long>(b) * p.v_sb +
+                           static_cast<long long>(h) * p.v_sh;
+        uint8_t *smem_gen = smem_raw + (base - raw);
+        for (int j = 0; j < n_kv; ++j) {
+            const int st = j % p.stages;
+            const int use = j / p.stages;
+            if (use > 0) {
+                bool ok = wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl, p);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            uint8_t *dst = smem_gen + (sV(st) - base);
+            for (int idx = lt; idx < BN * nd4; idx += C::kVLoaders) {
+                const int key = idx / nd4;
+                const int d0 = (idx - key * nd4) * 4;
+                const int kg = j * BN + key;
+                float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kg < p.S_k && d0 < p.D_v) {
+                    const float *src = vbh + static_cast<long long>(kg) * p.v_ss + d0;
+                    if (d0 + 4 <= p.D_v) {
+                        val = __ldg(reinterpret_cast<const float4 *>(src));
+                    } else {
+                        val.x = __ldg(src);
+                        if (d0 + 1 < p.D_v) val.y = __ldg(src + 1);
+                        if (d0 + 2 < p.D_v) val.z = __ldg(src + 2);
+                    }
+                }
+                uint8_t *chunk = dst + (key >> 5) * p.n_pv * 128;
+                const int kb = (key & 31) * 4;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 0, kb)) = val.x;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 1, kb)) = val.y;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 2, kb)) = val.z;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 3, kb)) = val.w;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(smem_u32(&ctl.full_v[st]));
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroup

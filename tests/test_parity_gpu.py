@@ -145,7 +145,7 @@ def test_write_set_guard_bands(dtype, causal):
     sentinel = SENT16 - (1 << 16) if dtype == "bf16" else SENT32
     buf = torch.full((total,), sentinel, dtype=tdt, device="cuda")
     view_dt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    O = torch.as_strided(buf.view(view_dt), (B, H, S_q, D_v), o_strides, canary + row)  # starts after one pad row
+    O = torch.as_strided(buf.view(view_dt), (B, H, S_q, D_v), o_strides + (1,), canary + row)  # after one pad row
     Q, K, V = to_device(q), to_device(k), to_device(v)
     vt.attn_fwd(Q, K, V, scale=0.2, causal=causal, out=O)
     assert vt.vt_last_device_status() == 0
