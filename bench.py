@@ -40,7 +40,8 @@ import synth  # noqa: E402
 METRIC = "attention fwd TFLOP/s (causal-adjusted) and % of GB300 dense tensor peak"
 DEFAULT_WORKLOAD = "bf16_causal_8k_peaky"
 KERNEL_SOURCES = [os.path.join(ROOT, "scaled_dot_product_vt_gb300", "csrc", f)
-                  for f in ("vt_attn_kernel.cuh", "vt_ptx.cuh", "vt_attn_api.cu")]
+                  for f in ("vt_attn_kernel.cuh", "vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_ptx.cuh",
+                            "vt_attn_api.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
 # nominal dense tf32 : bf16 tensor ratio (1.1 : 2.25 PFLOP/s), applied to the measured bf16 peak
 TF32_OVER_BF16 = 1.1 / 2.25
@@ -352,7 +353,7 @@ def main() -> int:
                          "frac": achieved / peak, "traffic": load_traffic(w.name),
                          "peak_source": (f"{peaks['source']} bf16 burst" if w.dtype == "bf16"
                                          else f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio"),
-                         "kernel": f"vt::attn_fwd_kernel<{'1' if w.dtype == 'bf16' else '0'}>",
+                         "kernel": "vt::attn_fwd_bf16_2q_kernel" if w.dtype == "bf16" else "vt::attn_fwd_kernel<0>",
                          "launch_ms": per_launch_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/vt_attn.h"
+#include "vt_attn_bf16_2q.cuh"
 #include "vt_attn_kernel.cuh"
 
 namespace vt {
@@ -83,10 +84,12 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
                  int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, cudaStream_t stream) {
     using C = Cfg<DT>;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, C::kBN))
+    // K/V boxes are one key tile high
+    const int kv_rows = DT == kBF16 ? q2::kBN : C::kBN;
+    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, kv_rows))
         return VT_ERR_CUDA;
     if (DT == kBF16) {
-        if (!make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, C::kBN)) return VT_ERR_CUDA;
+        if (!make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, kv_rows)) return VT_ERR_CUDA;
     } else {
         tv = tk;  // fp32: V is read by the kernel's transposing loader warps, not by TMA
     }
@@ -116,6 +119,43 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     p.flags = opts ? opts->flags : 0u;
 
+    void *status_ptr = nullptr;
+    if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return VT_ERR_CUDA;
+    p.status = static_cast<unsigned *>(status_ptr);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return VT_ERR_CUDA;
+
+    if (DT == kBF16) {
+        // two 128-row query tiles per CTA, 128-key tiles through a ring of equal K/V slots
+        p.n_qblocks = static_cast<int>((S_q + q2::kRows - 1) / q2::kRows);
+        const int q_bytes = 2 * p.q_chunks * static_cast<int>(q2::kChunkBytes);
+        const int slot_bytes = (p.q_chunks > p.v_chunks ? p.q_chunks : p.v_chunks) * static_cast<int>(q2::kChunkBytes);
+        const int budget = kSmemLimit - 1024 - static_cast<int>(sizeof(q2::Ctl)) - 256;
+        p.stages = (budget - q_bytes) / slot_bytes;  // number of slots
+        if (p.stages > q2::kMaxSlots) p.stages = q2::kMaxSlots;
+        if (p.stages < 2) return VT_ERR_UNSUPPORTED;
+        const int smem = 1024 + q_bytes + p.stages * slot_bytes;
+        // Interleave the query blocks of about two waves' worth of heads, so the CTAs in flight
+        // share their heads' K and V in L2.
+        const long long bh = B * H;
+        long long grp = (2LL * sms + p.n_qblocks - 1) / p.n_qblocks;
+        p.head_group = static_cast<int>(grp < 1 ? 1 : (grp > bh ? bh : grp));
+        const long long items = static_cast<long long>(p.n_qblocks) * bh;
+        if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        // Q K^T K-steps of 16, rounded up to an even count (the TMA zero-fills past D_qk)
+        const int ksteps = static_cast<int>((D_qk + 15) / 16);
+        void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
+            ksteps <= 2 ? attn_fwd_bf16_2q_kernel<2>
+                        : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4>
+                                      : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6> : attn_fwd_bf16_2q_kernel<8>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return VT_ERR_CUDA;
+        kern<<<static_cast<unsigned>(items), q2::kThreads, smem, stream>>>(tq, tk, tv, p);
+        if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+        return VT_OK;
+    }
+
     const int q_bytes = p.q_chunks * kBM * 128;
     const int kv_bytes = p.q_chunks * C::kBN * 128 + v_stage_bytes<DT>(p.v_chunks, p.n_pv);
     const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
@@ -123,10 +163,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return VT_ERR_UNSUPPORTED;
     const int smem = 1024 + q_bytes + p.stages * kv_bytes;
-
-    void *status_ptr = nullptr;
-    if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return VT_ERR_CUDA;
-    p.status = static_cast<unsigned *>(status_ptr);
+    p.head_group = 1;
 
     auto kern = attn_fwd_kernel<DT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

@@ -1,0 +1,443 @@
+// Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per CTA sharing every
+// 128-key K/V tile, one softmax warpgroup per query tile, single-thread tcgen05 issue.
+//
+// One CTA computes 256 query rows of one (b, h) slice as query tiles t = 0, 1 (rows
+// r0 + 128 t .. r0 + 128 t + 127).  Warp roles (12 warps, three warpgroups):
+//   warp 0       TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring of
+//                equal shared-memory slots (mbarrier full/empty per slot).
+//   warp 1       TMEM owner and MMA issuer (one thread).  Per key tile j the tensor core runs
+//                  O_0 += P_0,j V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1,j V_j,  S_1 = Q_1 K_{j+1}^T
+//                so while softmax warpgroup t works on S_t, the tensor core works for the other
+//                tile.  Every operand descriptor is computed once; the K-steps are unrolled
+//                (a per-instruction descriptor computation made the issuing thread, not the
+//                tensor core, the bottleneck).
+//   warps 2-3    idle (they complete warpgroup 0, which gives registers to the softmax warpgroups)
+//   warps 4-7    softmax warpgroup of tile 0, one row per thread (TMEM lane quadrant = warp % 4)
+//   warps 8-11   softmax warpgroup of tile 1
+// Registers: launched at 168 per thread; warpgroup 0 shrinks to 56 and the softmax warpgroups
+// grow to 224 (128 x 56 + 256 x 224 = 384 x 168, so the increase never waits on a shortfall).
+// TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.  P_t,j overwrites S_t,j as bf16
+// pairs (64 columns) and is read from TMEM by the P V product.  A commit after S_t = Q_t K^T
+// also covers the P V issued before it, so when softmax t sees its next scores, O_t is final
+// for the previous tile and may be rescaled in place.
+//
+// The decomposition (query block, head, batch), the tail masks and the write set follow the
+// FA-1 boundary kernel verified on the VeriTile page "VeriTile.Examples.FlashAttention1.
+// NaiveRefinement"; the reductions are the accy page's score_dot, score_max, score_exp_sum and
+// value_weighted_sum, computed online with the base-2 exponential of the folded scale.
+#pragma once
+
+#include "vt_attn_common.cuh"
+
+namespace vt {
+namespace q2 {
+
+constexpr int kBN = 128;            // keys per tile
+constexpr int kRows = 256;          // query rows per CTA
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kRegsControl = 64;    // warpgroup 0 after setmaxnreg
+constexpr int kRegsSoftmax = 216;   // softmax warpgroups after setmaxnreg
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch");
+constexpr int kMaxSlots = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kChunk = 64;          // bf16 elements per 128-byte chunk
+constexpr uint32_t kChunkBytes = kBN * 128;  // one 128-byte column chunk of a 128-row tile
+
+__host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t * 128); }
+__host__ __device__ constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
+
+struct Ctl {
+    uint64_t full[kMaxSlots];
+    uint64_t empty[kMaxSlots];
+    uint64_t q_full;
+    uint64_t s_full[2];   // scores of tile t ready (and every earlier MMA done)
+    uint64_t p_full[2];   // P of tile t written (128 arrivals)
+    uint64_t o_done[2];   // last P V of tile t done
+    uint64_t drain;
+    uint64_t stall;
+    uint32_t tmem_base;
+    volatile uint32_t abort_flag;
+};
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+}  // namespace q2
+
+// KQ: MMA K-steps (16 bf16 each) of Q K^T, D_qk rounded up: 2, 4, 6 or 8.
+template <int KQ>
+__global__ void __launch_bounds__(q2::kThreads, 1)
+    attn_fwd_bf16_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using namespace q2;
+    constexpr int BN = kBN;
+    __shared__ Ctl ctl;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- work item: groups of `head_group` heads; inside a group, heavy causal blocks first
+    const int BH = p.B * p.H;
+    const int per_group = p.head_group * p.n_qblocks;
+    const int g = blockIdx.x / per_group;
+    const int rr = blockIdx.x - g * per_group;
+    const int g_heads = min(p.head_group, BH - g * p.head_group);
+    const int slot_q = rr / g_heads;
+    const int bh = g * p.head_group + (rr - slot_q * g_heads);
+    const int qb = p.causal ? (p.n_qblocks - 1 - slot_q) : slot_q;
+    const int h = bh % p.H;
+    const int b = bh / p.H;
+    const int r0 = qb * kRows;
+
+    // key tiles each query tile needs (0 when the tile lies past S_q)
+    const int n_all = (p.S_k + BN - 1) / BN;
+    int n0, n1;
+    {
+        int n[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int first = r0 + t * kBM;
+            if (first >= p.S_q) n[t] = 0;
+            else if (p.causal) n[t] = min(n_all, (min(first + kBM, p.S_q) - 1) / BN + 1);
+            else n[t] = n_all;
+        }
+        n0 = n[0];
+        n1 = n[1];
+    }
+    const int n_kv = max(n0, n1);
+    const int n_slots = p.stages;
+
+    // ---- shared memory: Q tile 0, Q tile 1, then `n_slots` equal K/V slots
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t q_tile_bytes = p.q_chunks * kChunkBytes;
+    const uint32_t k_bytes = p.q_chunks * kChunkBytes;
+    const uint32_t v_bytes = p.v_chunks * kChunkBytes;
+    const uint32_t slot_bytes = max(k_bytes, v_bytes);
+    const uint32_t sQ0 = base, sQ1 = base + q_tile_bytes;
+    const uint32_t sSlot0 = base + 2 * q_tile_bytes;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < n_slots; ++s) {
+            mbar_init(smem_u32(&ctl.full[s]), 1);
+            mbar_init(smem_u32(&ctl.empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl.q_full), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&ctl.s_full[t]), 1);
+            mbar_init(smem_u32(&ctl.p_full[t]), 128);
+            mbar_init(smem_u32(&ctl.o_done[t]), 1);
+        }
+        mbar_init(smem_u32(&ctl.drain), 1);
+        mbar_init(smem_u32(&ctl.stall), 1);
+        ctl.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const int q_tiles = n1 > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_tiles * q_tile_bytes);
+            for (int c = 0; c < p.q_chunks; ++c)
+                tma_load_4d(sQ0 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0, h, b);
+            if (q_tiles == 2)
+                for (int c = 0; c < p.q_chunks; ++c)
+                    tma_load_4d(sQ1 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0 + kBM, h, b);
+            // loads i = 2j (K_j) and 2j + 1 (V_j) go to slot i mod n_slots
+            int s = 0;
+            uint32_t empty_phase = 0;  // bit s: parity of the next empty-phase of slot s to wait for
+            int loads = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < 2 * n_kv; ++i) {
+                if (loads >= n_slots) {
+                    ok = wait_bounded(smem_u32(&ctl.empty[s]), (empty_phase >> s) & 1u, ctl.abort_flag, p);
+                    empty_phase ^= 1u << s;
+                    if (!ok) break;
+                }
+                const uint32_t dst = sSlot0 + s * slot_bytes;
+                const uint32_t bar = smem_u32(&ctl.full[s]);
+                const int j = i >> 1;
+                if ((i & 1) == 0) {
+                    mbar_arrive_expect_tx(bar, k_bytes);
+                    for (int c = 0; c < p.q_chunks; ++c)
+                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, j * BN, h, b);
+                } else {
+                    mbar_arrive_expect_tx(bar, v_bytes);
+                    for (int c = 0; c < p.v_chunks; ++c)
+                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, j * BN, h, b);
+                }
+                ++loads;
+                if (++s == n_slots) s = 0;
+            }
+            if (ctl.abort_flag) {
+                // Let every copy this thread started land before the CTA's memory goes away:
+                // the last min(loads, n_slots) loads, one per slot, each on the full phase it used.
+                wait_drain(smem_u32(&ctl.q_full), 0, p);
+                for (int k = max(0, loads - n_slots); k < loads; ++k)
+                    wait_drain(smem_u32(&ctl.full[k % n_slots]), (k / n_slots) & 1, p);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = instr_desc(1, kBM, BN, 0);
+            const uint32_t idesc_pv = instr_desc(1, kBM, p.n_pv, 1);
+            // Descriptors as (low, high) words: offsets only move the low word (start address >> 4).
+            const uint64_t qdesc0 = smem_desc_sw128(sQ0, 16, 1024);
+            const uint64_t kdesc0 = smem_desc_sw128(sSlot0, 16, 1024);         // K slots: K-major
+            const uint64_t vdesc0 = smem_desc_sw128(sSlot0, kChunkBytes, 1024);  // V slots: N-major
+            const uint32_t q_hi = static_cast<uint32_t>(qdesc0 >> 32), k_hi = static_cast<uint32_t>(kdesc0 >> 32);
+            const uint32_t v_hi = static_cast<uint32_t>(vdesc0 >> 32);
+            const uint32_t q_lo0 = static_cast<uint32_t>(qdesc0);
+            const uint32_t q_lo1 = q_lo0 + (q_tile_bytes >> 4);
+            const uint32_t k_lo0 = static_cast<uint32_t>(kdesc0), v_lo0 = static_cast<uint32_t>(vdesc0);
+            const uint32_t slot_step = slot_bytes >> 4;                          // descriptor units
+            const uint32_t s_col0 = tmem + col_s(0), s_col1 = tmem + col_s(1);
+            const uint32_t o_col0 = tmem + col_o(0), o_col1 = tmem + col_o(1);
+            bool ok = true, any_mma = false;
+            uint32_t full_phase = 0;  // bit s: parity of the next full-phase of slot s
+
+            auto wait_full = [&](int s) -> bool {
+                const bool r = wait_bounded(smem_u32(&ctl.full[s]), (full_phase >> s) & 1u, ctl.abort_flag, p);
+                full_phase ^= 1u << s;
+                tc_fence_after();
+                return r;
+            };
+            auto qk = [&](uint32_t d, uint32_t q_lo, uint32_t k_lo) {
+#pragma unroll
+                for (int kk = 0; kk < KQ; ++kk) {
+                    const uint32_t off = (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2;
+                    mma_ss_w(d, q_lo + off, q_hi, k_lo + off, k_hi, idesc_qk, kk > 0);
+                }
+            };
+            auto pv = [&](uint32_t d, uint32_t a, uint32_t v_lo, uint32_t acc0) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts_w(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u);
+            };
+
+            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook
+            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
+            int ks = 0;  // slot of K_j
+            if (ok) ok = wait_full(ks);
+            if (ok) {
+                const uint32_t k_lo = k_lo0 + ks * slot_step;
+                if (n0 > 0) {
+                    qk(s_col0, q_lo0, k_lo);
+                    mma_commit(smem_u32(&ctl.s_full[0]));
+                }
+                if (n1 > 0) {
+                    qk(s_col1, q_lo1, k_lo);
+                    mma_commit(smem_u32(&ctl.s_full[1]));
+                }
+                mma_commit(smem_u32(&ctl.empty[ks]));
+                any_mma = true;
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int vs = ks + 1 == n_slots ? 0 : ks + 1;  // slot of V_j
+                const int kn = vs + 1 == n_slots ? 0 : vs + 1;  // slot of K_{j+1}
+                const bool more = j + 1 < n_kv;
+                if (!(ok = wait_full(vs))) break;
+                const uint32_t v_lo = v_lo0 + vs * slot_step;
+                const uint32_t kn_lo = k_lo0 + kn * slot_step;
+                if (j < n0) {
+                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), j & 1, ctl.abort_flag, p))) break;
+                    tc_fence_after();
+                    pv(o_col0, s_col0, v_lo, j > 0);
+                }
+                if (more && !(ok = wait_full(kn))) break;
+                if (j + 1 < n0) {
+                    qk(s_col0, q_lo0, kn_lo);
+                    mma_commit(smem_u32(&ctl.s_full[0]));
+                } else if (j < n0) {
+                    mma_commit(smem_u32(&ctl.o_done[0]));
+                }
+                if (j < n1) {
+                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), j & 1, ctl.abort_flag, p))) break;
+                    tc_fence_after();
+                    pv(o_col1, s_col1, v_lo, j > 0);
+                }
+                mma_commit(smem_u32(&ctl.empty[vs]));
+                if (j + 1 < n1) {
+                    qk(s_col1, q_lo1, kn_lo);
+                    mma_commit(smem_u32(&ctl.s_full[1]));
+                } else if (j < n1) {
+                    mma_commit(smem_u32(&ctl.o_done[1]));
+                }
+                if (more) mma_commit(smem_u32(&ctl.empty[kn]));
+                ks = kn;
+            }
+            if (!ok && any_mma) {
+                mma_commit(smem_u32(&ctl.drain));
+                wait_drain(smem_u32(&ctl.drain), 0, p);
+            }
+        }
+    }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        const int t = (warp - 4) >> 2;              // query tile of this warpgroup
+        const int quad = warp & 3;                  // TMEM lane quadrant
+        const int row = quad * 32 + lane;
+        const int tile_row0 = r0 + t * kBM;
+        const int q_row = tile_row0 + row;
+        const int n_my = t ? n1 : n0;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + col_s(t);
+        const uint32_t o_addr = tmem + lane_base + col_o(t);
+        // Non-positive scales are applied to the scores first, so the folded form below sees c > 0.
+        const bool fold = p.scale_log2 > 0.0f;
+        const float c = fold ? p.scale_log2 : 1.0f;
+        const float2 c2 = make_float2(c, c);
+        float m_used = -INFINITY;  // reference max (log2 units) of O_t and l
+        float l = 0.0f;
+        bool ok = true;
+
+        for (int j = 0; j < n_my; ++j) {
+            ok = wait_bounded(smem_u32(&ctl.s_full[t]), j & 1, ctl.abort_flag, p);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[BN];
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+            tmem_wait_ld();
+            float s[BN];
+#pragma unroll
+            for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
+            if (!fold) {
+#pragma unroll
+                for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
+            }
+            const int k0 = j * BN;
+            if ((k0 + BN > p.S_k) || (p.causal && k0 + BN - 1 > tile_row0)) {
+                const int lim = p.causal ? min(p.S_k, q_row + 1) : p.S_k;  // keys k0+k < lim are allowed
+#pragma unroll
+                for (int k = 0; k < BN; ++k)
+                    if (k0 + k >= lim) s[k] = -INFINITY;
+            }
+            float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+            float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+            for (int k = 12; k < BN - 4; k += 8) {
+                mx0 = fmax3(mx0, s[k], s[k + 1]);
+                mx1 = fmax3(mx1, s[k + 2], s[k + 3]);
+                mx2 = fmax3(mx2, s[k + 4], s[k + 5]);
+                mx3 = fmax3(mx3, s[k + 6], s[k + 7]);
+            }
+            mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+            mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+            const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;  // c > 0: -inf stays -inf
+            const float m_new = fmaxf(m_used, m_tile);
+            // Lazy rescale: keep the old reference unless the max grew by more than tau.
+            const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kRescaleTau);
+            float alpha = 1.0f;
+            if (resc) {
+                alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);
+                l *= alpha;
+                m_used = m_new;
+            }
+            const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+            // P_t,j over S_t,j (bf16 pairs): each 32-score chunk goes to TMEM as 16 columns as
+            // soon as it is exponentiated, which keeps the live registers near the 128 scores.
+#pragma unroll
+            for (int cc = 0; cc < BN; cc += 32) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    const float2 x0 = __ffma2_rn(make_float2(s[cc + k], s[cc + k + 1]), c2, nm2);
+                    const float2 x1 = __ffma2_rn(make_float2(s[cc + k + 2], s[cc + k + 3]), c2, nm2);
+                    const float2 e0 = make_float2(ex2(x0.x), ex2(x0.y));
+                    const float2 e1 = make_float2(ex2(x1.x), ex2(x1.y));
+                    acc0 = __fadd2_rn(acc0, e0);
+                    acc1 = __fadd2_rn(acc1, e1);
+                    pk[k / 2] = pack_bf16x2(e0.x, e0.y);
+                    pk[k / 2 + 1] = pack_bf16x2(e1.x, e1.y);
+                }
+                tmem_st16(s_addr + cc / 2, pk);
+            }
+            l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            // O_t *= alpha where the reference moved (after the scores are dead, to keep registers low).  The scores just read were committed after
+            // P_t,j-1 V_j-1, so O_t holds its final value for tile j-1 and no MMA touches it now.
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                for (int cc = 0; cc < p.n_pv; cc += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + cc, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st32(o_addr + cc, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl.p_full[t]));
+        }
+
+        if (ok && n_my > 0) {
+            ok = wait_bounded(smem_u32(&ctl.o_done[t]), 0, ctl.abort_flag, p);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                // ------------------------------------------------------------ epilogue
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                const bool row_ok = q_row < p.S_q;
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                                (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
+                                 static_cast<long long>(q_row) * p.o_ss) * 2;
+                for (int cc = 0; cc < p.n_pv; cc += 16) {
+                    uint32_t o[16];
+                    tmem_ld16(o_addr + cc, o);
+                    tmem_wait_ld();
+                    if (!row_ok) continue;
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                    if (cc + 16 <= p.D_v) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace vt

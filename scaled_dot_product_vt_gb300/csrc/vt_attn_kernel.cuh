@@ -24,38 +24,9 @@
 #include <cuda.h>
 #include <cstdint>
 
-#include "vt_ptx.cuh"
+#include "vt_attn_common.cuh"
 
 namespace vt {
-
-constexpr int kBM = 128;           // query rows per work item (= TMEM lanes)
-constexpr int kMaxStages = 4;
-constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
-
-// Device status bits (the host maps them to vt_status codes).
-constexpr unsigned kStatusTimeout = 1u;
-constexpr unsigned kStatusBounds = 2u;
-
-enum : int { kF32 = 0, kBF16 = 1 };
-
-struct AttnParams {
-    int B, H, S_q, S_k, D_qk, D_v;
-    int n_qblocks;    // ceil(S_q / 128)
-    int qk_ksteps;    // ceil(D_qk / K-step), K-step = 16 (bf16) or 8 (tf32)
-    int q_chunks;     // 128-byte column chunks of a Q/K row: ceil(D_qk * elt / 128)
-    int v_chunks;     // 128-byte column chunks of a V row
-    int n_pv;         // MMA N of P*V: D_v rounded up to 16
-    int stages;
-    int causal;
-    float scale_log2;  // scale * log2(e)
-    void *O;
-    long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
-    const void *V;               // read by the fp32 V loader
-    long long v_sb, v_sh, v_ss;
-    unsigned long long timeout_ns;
-    unsigned flags;
-    unsigned *status;  // device status word
-};
 
 template <int DT>
 struct Cfg {
@@ -96,35 +67,6 @@ struct SharedCtl {
     uint32_t tmem_base;
     volatile uint32_t abort_flag;
 };
-
-// Wait for the phase of `bar` with `parity`, giving up after the time limit or when
-// another role has aborted.  Returns false on give-up (after flagging the abort).
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, SharedCtl &ctl, const AttnParams &p) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63u) == 0) {
-            if (ctl.abort_flag) return false;
-            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                ctl.abort_flag = 1;
-                atomicOr(p.status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// Wait without the abort shortcut (used while draining copies in flight on the abort path).
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const AttnParams &p) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > p.timeout_ns) {
-            atomicOr(p.status, kStatusTimeout);
-            return;
-        }
-    }
-}
 
 template <int DT>
 __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
@@ -204,7 +146,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j % p.stages;
                 const int use = j / p.stages;
-                if (use > 0 && !wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl, p)) break;
+                if (use > 0 && !wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl.abort_flag, p)) break;
                 mbar_arrive_expect_tx(smem_u32(&ctl.full_k[st]), k_bytes);
                 for (int c = 0; c < p.q_chunks; ++c)
                     tma_load_4d(sK(st) + c * BN * 128, &tmK, smem_u32(&ctl.full_k[st]), c * C::kChunkElems, j * BN,
@@ -233,13 +175,13 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, DT == kBF16 ? 1 : 0);
             bool ok = true, any_mma = false;
-            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl, p);  // test hook: never signalled
-            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl, p);
+            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook: never signalled
+            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
             tc_fence_after();
 
             auto issue_qk = [&](int j) -> bool {
                 const int st = j % p.stages;
-                if (!wait_bounded(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, ctl, p)) return false;
+                if (!wait_bounded(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, ctl.abort_flag, p)) return false;
                 tc_fence_after();
                 const uint32_t d = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
                 for (int kk = 0; kk < p.qk_ksteps; ++kk) {
@@ -258,8 +200,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
                 const int st = j % p.stages;
-                if (!wait_bounded(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, ctl, p)) { ok = false; break; }
-                if (!wait_bounded(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, ctl, p)) { ok = false; break; }
+                if (!wait_bounded(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, ctl.abort_flag, p)) { ok = false; break; }
+                if (!wait_bounded(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, ctl.abort_flag, p)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_base = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
                 for (int kk = 0; kk < BN / C::kKStep; ++kk) {
@@ -293,7 +235,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             const int st = j % p.stages;
             const int use = j / p.stages;
             if (use > 0) {
-                bool ok = wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl, p);
+                bool ok = wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl.abort_flag, p);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             }
@@ -335,7 +277,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         bool ok = true;
 
         for (int j = 0; j < n_kv; ++j) {
-            ok = wait_bounded(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, ctl, p);
+            ok = wait_bounded(smem_u32(&ctl.s_full[j & 1]), (j >> 1) & 1, ctl.abort_flag, p);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -406,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
 
             // O *= alpha for rows whose reference moved, once P_{j-1} V_{j-1} has landed.
             if (j > 0) {
-                ok = wait_bounded(smem_u32(&ctl.o_done), (j - 1) & 1, ctl, p);
+                ok = wait_bounded(smem_u32(&ctl.o_done), (j - 1) & 1, ctl.abort_flag, p);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -428,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
 
         if (ok) {
-            ok = wait_bounded(smem_u32(&ctl.o_done), (n_kv - 1) & 1, ctl, p);
+            ok = wait_bounded(smem_u32(&ctl.o_done), (n_kv - 1) & 1, ctl.abort_flag, p);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
