@@ -42,6 +42,11 @@ constexpr int kMaxSlots = 6;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunk = 64;          // bf16 elements per 128-byte chunk
 constexpr uint32_t kChunkBytes = kBN * 128;  // one 128-byte column chunk of a 128-row tile
+// Lazy-rescale threshold (log2 units).  P <= 2^32 is exact-range safe in bf16 (fp32 exponent
+// range), and O and l accumulate in fp32 with room to spare (2^32 * |V| * S_k << 2^128); the
+// relative precision of P, O and l does not depend on their scale.  A large threshold means the
+// O rescale essentially only happens when a row's max jumps by more than 2^32.
+constexpr float kTau = 32.0f;
 
 __host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t * 128); }
 __host__ __device__ constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;  // c > 0: -inf stays -inf
             const float m_new = fmaxf(m_used, m_tile);
             // Lazy rescale: keep the old reference unless the max grew by more than tau.
-            const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kRescaleTau);
+            const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kTau);
             float alpha = 1.0f;
             if (resc) {
                 alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);

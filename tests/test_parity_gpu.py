@@ -110,6 +110,31 @@ def test_unusual_scales(scale):
         check(run(q, k, v, scale, causal), oracle.attn_fwd(q, k, v, scale, causal), "bf16", f"scale={scale}")
 
 
+def _tf32_exact(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the 10-bit mantissa the TF32 tensor path reads (nearest, ties away)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_path(dtype, causal):
+    """Key norms grow along the sequence, so each row's running max keeps jumping by more than the
+    lazy-rescale threshold: the O-rescale path runs on most key tiles.  Inputs are exactly
+    representable in the tensor path's input precision (bf16, or TF32 for fp32 I/O), so the
+    comparison checks the rescale logic rather than input rounding at these very large scores."""
+    B, H, S_q, S_k, D = 1, 2, 300, 700, 64
+    q, k, v = synth.make_qkv(B, H, S_q, S_k, D, D, "f32", sigma_q=3.0, seed=17)
+    growth = (1.0 + np.arange(S_k, dtype=np.float32) / 16.0)[None, None, :, None]
+    k = (k * growth).astype(np.float32)
+    if dtype == "bf16":
+        q, k, v = (synth.to_bf16_bits(x) for x in (q, k, v))
+    else:
+        q, k, v = (_tf32_exact(x) for x in (q, k, v))
+    scale = float(np.float32(0.125))  # a power of two: exact in any precision
+    check(run(q, k, v, scale, causal), oracle.attn_fwd(q, k, v, scale, causal), dtype, "rescale path")
+
+
 # ---------------------------------------------------------------- invariants on the GPU
 
 def test_gpu_ones_value_and_causal_row0():
