@@ -222,10 +222,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             bool ok = true, any_mma = false;
             uint32_t full_phase = 0;  // bit s: parity of the next full-phase of slot s
 
+            // K/V slots are filled by TMA: the mbarrier's completed transaction count already makes
+            // the bytes visible to the tensor core, so no tcgen05 fence is needed after this wait.
             auto wait_full = [&](int s) -> bool {
                 const bool r = wait_bounded(smem_u32(&ctl.full[s]), (full_phase >> s) & 1u, ctl.abort_flag, p);
                 full_phase ^= 1u << s;
-                tc_fence_after();
                 return r;
             };
             auto qk = [&](uint32_t d, uint32_t q_lo, uint32_t k_lo) {
