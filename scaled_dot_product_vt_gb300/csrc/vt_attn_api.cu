@@ -126,7 +126,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return VT_ERR_CUDA;
 
-    if (DT == kBF16) {
+    if constexpr (DT == kBF16) {
         // two 128-row query tiles per CTA, 128-key tiles through a ring of equal K/V slots
         p.n_qblocks = static_cast<int>((S_q + q2::kRows - 1) / q2::kRows);
         const int q_bytes = 2 * p.q_chunks * static_cast<int>(q2::kChunkBytes);
@@ -154,25 +154,30 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
         kern<<<static_cast<unsigned>(items), q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
         return VT_OK;
+    } else {
+        // one 128-row query tile per CTA (fp32 I/O on the TF32 path)
+        const int q_bytes = p.q_chunks * kBM * 128;
+        const int kv_bytes = p.q_chunks * C::kBN * 128 + v_stage_bytes<DT>(p.v_chunks, p.n_pv);
+        const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
+        p.stages = (budget - q_bytes) / kv_bytes;
+        if (p.stages > kMaxStages) p.stages = kMaxStages;
+        if (p.stages < 2) return VT_ERR_UNSUPPORTED;
+        const int smem = 1024 + q_bytes + p.stages * kv_bytes;
+        p.head_group = 1;
+        // Q K^T K-steps of 8 tf32, rounded up to whole 128-byte chunks (the TMA zero-fills past D_qk)
+        const int chunks = p.q_chunks;
+        void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
+            chunks <= 1 ? attn_fwd_kernel<DT, 4>
+                        : chunks == 2 ? attn_fwd_kernel<DT, 8>
+                                      : chunks == 3 ? attn_fwd_kernel<DT, 12> : attn_fwd_kernel<DT, 16>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return VT_ERR_CUDA;
+        const long long items = static_cast<long long>(p.n_qblocks) * B * H;
+        if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
+        if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+        return VT_OK;
     }
-
-    const int q_bytes = p.q_chunks * kBM * 128;
-    const int kv_bytes = p.q_chunks * C::kBN * 128 + v_stage_bytes<DT>(p.v_chunks, p.n_pv);
-    const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
-    p.stages = (budget - q_bytes) / kv_bytes;
-    if (p.stages > kMaxStages) p.stages = kMaxStages;
-    if (p.stages < 2) return VT_ERR_UNSUPPORTED;
-    const int smem = 1024 + q_bytes + p.stages * kv_bytes;
-    p.head_group = 1;
-
-    auto kern = attn_fwd_kernel<DT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return VT_ERR_CUDA;
-    const long long items = static_cast<long long>(p.n_qblocks) * B * H;
-    if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
-    kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
-    return VT_OK;
 }
 
 vt_status read_status(cudaStream_t stream) {

@@ -47,9 +47,8 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
-        // Suspended rather than spinning: a waiting warp leaves its issue slots to the others.
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-        if ((n & 3u) == 0) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
             if (abort_flag) return false;
             if (globaltimer_ns() - t0 > p.timeout_ns) {
                 abort_flag = 1;

@@ -8,7 +8,7 @@
 //   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
 //               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
 //               over S_j, O rescale when the reference max moves, and the epilogue.
-//   warps 6-7   fp32 I/O only: V loader.  The TF32 MMA takes its B operand K-major only (an
+//   warps 6-9   fp32 I/O only: V loader.  The TF32 MMA takes its B operand K-major only (an
 //               N-major tf32 B reads as zeros), so V tiles are read with coalesced 16-byte
 //               loads and written transposed (keys contiguous) into the 128-byte-swizzled
 //               K-major layout; for bf16, V goes by TMA as it is (N-major B).
@@ -37,8 +37,10 @@ struct Cfg {
     static constexpr uint32_t kFmt = DT == kBF16 ? 1u : 2u;    // bf16 / tf32
     static constexpr uint32_t kTmemCols = DT == kBF16 ? 512u : 256u;
     static constexpr uint32_t kColS0 = 0, kColS1 = kBN, kColO = 2 * kBN;
-    static constexpr int kThreads = DT == kBF16 ? 192 : 256;
-    static constexpr int kVLoaders = DT == kBF16 ? 0 : 64;
+    static constexpr int kThreads = DT == kBF16 ? 192 : 320;
+    static constexpr int kVLoaders = DT == kBF16 ? 0 : 128;
+    // float4 loads per loader thread and V tile, at most (BN keys x 128 columns / 4 / loaders)
+    static constexpr int kVLoadsPerThread = DT == kBF16 ? 1 : (64 * 128 / 4) / 128;
 };
 
 // Bytes of one V stage: bf16 keeps V N-major (128-byte column chunks of BN key rows); fp32
@@ -68,7 +70,8 @@ struct SharedCtl {
     volatile uint32_t abort_flag;
 };
 
-template <int DT>
+// KQ: MMA K-steps (8 tf32 each) of Q K^T, D_qk rounded up to a whole 128-byte chunk: 4, 8, 12 or 16.
+template <int DT, int KQ>
 __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -171,26 +174,33 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Descriptors are built once as (low, high) words and the K-steps are unrolled (KQ):
+        // computing a descriptor per instruction would make this thread the bottleneck.
         if (lane == 0) {
+            static_assert(DT == kF32, "this kernel serves fp32 I/O; bf16 uses the two-tile kernel");
             const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
-            const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, DT == kBF16 ? 1 : 0);
+            const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, 0);
+            const uint64_t qdesc = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t kdesc0 = smem_desc_sw128(sK(0), 16, 1024);
+            const uint64_t vdesc0 = smem_desc_sw128(sV(0), 16, 1024);  // V^T, K-major
+            const uint32_t q_lo = static_cast<uint32_t>(qdesc), q_hi = static_cast<uint32_t>(qdesc >> 32);
+            const uint32_t k_lo0 = static_cast<uint32_t>(kdesc0), k_hi = static_cast<uint32_t>(kdesc0 >> 32);
+            const uint32_t v_lo0 = static_cast<uint32_t>(vdesc0), v_hi = static_cast<uint32_t>(vdesc0 >> 32);
+            const uint32_t stage_step = (k_bytes + v_bytes) >> 4;
+            const uint32_t v_chunk = static_cast<uint32_t>(p.n_pv) * 8;  // one V^T key chunk, descriptor units
             bool ok = true, any_mma = false;
             if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook: never signalled
             if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
-            tc_fence_after();
 
             auto issue_qk = [&](int j) -> bool {
                 const int st = j % p.stages;
                 if (!wait_bounded(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, ctl.abort_flag, p)) return false;
-                tc_fence_after();
                 const uint32_t d = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
-                for (int kk = 0; kk < p.qk_ksteps; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kBM * 128 + off, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sK(st) + (kk >> 2) * BN * 128 + off, 16, 1024);
-                    if (DT == kBF16) mma_ss(d, a, bd, idesc_qk, kk > 0);
-                    else mma_ss_tf32(d, a, bd, idesc_qk, kk > 0);
-                }
+                const uint32_t k_lo = k_lo0 + st * stage_step;
+#pragma unroll
+                for (int kk = 0; kk < KQ; ++kk)
+                    mma_ss_tf32_w(d, q_lo + (kk >> 2) * (kBM * 8) + (kk & 3) * 2, q_hi,
+                                  k_lo + (kk >> 2) * (BN * 8) + (kk & 3) * 2, k_hi, idesc_qk, kk > 0);
                 mma_commit(smem_u32(&ctl.s_full[j & 1]));
                 any_mma = true;
                 return true;
@@ -202,20 +212,14 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 const int st = j % p.stages;
                 if (!wait_bounded(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, ctl.abort_flag, p)) { ok = false; break; }
                 if (!wait_bounded(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, ctl.abort_flag, p)) { ok = false; break; }
-                tc_fence_after();
+                tc_fence_after();  // P was written to TMEM and V^T to shared memory by other warps
                 const uint32_t a_base = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
-                for (int kk = 0; kk < BN / C::kKStep; ++kk) {
-                    if (DT == kBF16) {
-                        // V N-major: K-step = 16 key rows of 128 bytes; N chunks BN*128 bytes apart
-                        const uint64_t bd = smem_desc_sw128(sV(st) + kk * C::kKStep * 128, BN * 128, 1024);
-                        mma_ts(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
-                    } else {
-                        // V^T K-major: K-step = 8 keys = 32 bytes inside a 128-byte key chunk
-                        const uint64_t bd =
-                            smem_desc_sw128(sV(st) + (kk >> 2) * p.n_pv * 128 + (kk & 3) * 32, 16, 1024);
-                        mma_ts_tf32(tmem + C::kColO, a_base + kk * 8, bd, idesc_pv, (j > 0 || kk > 0));
-                    }
-                }
+                const uint32_t v_lo = v_lo0 + st * stage_step;
+                // V^T K-major: K-step = 8 keys = 32 bytes inside a 128-byte key chunk
+#pragma unroll
+                for (int kk = 0; kk < BN / C::kKStep; ++kk)
+                    mma_ts_tf32_w(tmem + C::kColO, a_base + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi,
+                                  idesc_pv, (j > 0 || kk > 0));
                 mma_commit(smem_u32(&ctl.empty[st]));
                 mma_commit(smem_u32(&ctl.o_done));
             }
@@ -240,27 +244,39 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 if (!ok) break;
             }
             uint8_t *dst = smem_gen + (sV(st) - base);
-            for (int idx = lt; idx < BN * nd4; idx += C::kVLoaders) {
+            // All of this thread's loads of the tile are issued before any store, so the tile
+            // costs one memory round trip rather than one per load.
+            float4 val[C::kVLoadsPerThread];
+#pragma unroll
+            for (int u = 0; u < C::kVLoadsPerThread; ++u) {
+                const int idx = lt + u * C::kVLoaders;
                 const int key = idx / nd4;
                 const int d0 = (idx - key * nd4) * 4;
                 const int kg = j * BN + key;
-                float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kg < p.S_k && d0 < p.D_v) {
+                val[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (idx < BN * nd4 && kg < p.S_k && d0 < p.D_v) {
                     const float *src = vbh + static_cast<long long>(kg) * p.v_ss + d0;
                     if (d0 + 4 <= p.D_v) {
-                        val = __ldg(reinterpret_cast<const float4 *>(src));
+                        val[u] = __ldg(reinterpret_cast<const float4 *>(src));
                     } else {
-                        val.x = __ldg(src);
-                        if (d0 + 1 < p.D_v) val.y = __ldg(src + 1);
-                        if (d0 + 2 < p.D_v) val.z = __ldg(src + 2);
+                        val[u].x = __ldg(src);
+                        if (d0 + 1 < p.D_v) val[u].y = __ldg(src + 1);
+                        if (d0 + 2 < p.D_v) val[u].z = __ldg(src + 2);
                     }
                 }
+            }
+#pragma unroll
+            for (int u = 0; u < C::kVLoadsPerThread; ++u) {
+                const int idx = lt + u * C::kVLoaders;
+                if (idx >= BN * nd4) break;
+                const int key = idx / nd4;
+                const int d0 = (idx - key * nd4) * 4;
                 uint8_t *chunk = dst + (key >> 5) * p.n_pv * 128;
                 const int kb = (key & 31) * 4;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 0, kb)) = val.x;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 1, kb)) = val.y;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 2, kb)) = val.z;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 3, kb)) = val.w;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 0, kb)) = val[u].x;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 1, kb)) = val[u].y;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 2, kb)) = val[u].z;
+                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 3, kb)) = val[u].w;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(smem_u32(&ctl.full_v[st]));
