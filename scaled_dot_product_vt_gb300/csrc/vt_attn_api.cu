@@ -46,6 +46,56 @@ bool env_check() {
     return on;
 }
 
+// Per-device facts that do not change while the process runs, looked up once: the SM count, the
+// device address of the status word, and the dynamic shared memory already granted per kernel.
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    unsigned *status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_info_mu;
+DeviceInfo g_info[kMaxDevices];
+struct SmemGrant {
+    const void *kern;
+    int dev;
+    int bytes;
+};
+SmemGrant g_grants[64];
+int g_n_grants = 0;
+
+bool device_info(int dev, DeviceInfo *out) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    DeviceInfo &d = g_info[dev];
+    if (!d.ready) {
+        void *status_ptr = nullptr;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return false;
+        d.status = static_cast<unsigned *>(status_ptr);
+        d.ready = true;
+    }
+    *out = d;
+    return true;
+}
+
+// cudaFuncSetAttribute for the dynamic shared memory size, only when a kernel needs more on a
+// device than it was granted before.
+bool ensure_smem(const void *kern, int dev, int bytes) {
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    for (int i = 0; i < g_n_grants; ++i)
+        if (g_grants[i].kern == kern && g_grants[i].dev == dev) {
+            if (g_grants[i].bytes >= bytes) return true;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+                return false;
+            g_grants[i].bytes = bytes;
+            return true;
+        }
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    if (g_n_grants < 64) g_grants[g_n_grants++] = {kern, dev, bytes};
+    return true;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -119,12 +169,11 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     p.flags = opts ? opts->flags : 0u;
 
-    void *status_ptr = nullptr;
-    if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return VT_ERR_CUDA;
-    p.status = static_cast<unsigned *>(status_ptr);
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return VT_ERR_CUDA;
+    int dev = 0;
+    DeviceInfo info;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_info(dev, &info)) return VT_ERR_CUDA;
+    p.status = info.status;
+    const int sms = info.sms;
 
     if constexpr (DT == kBF16) {
         // two 128-row query tiles per CTA, 128-key tiles through a ring of equal K/V slots
@@ -149,8 +198,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
             ksteps <= 2 ? attn_fwd_bf16_2q_kernel<2>
                         : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4>
                                       : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6> : attn_fwd_bf16_2q_kernel<8>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return VT_ERR_CUDA;
+        if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<static_cast<unsigned>(items), q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
         return VT_OK;
@@ -170,8 +218,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
             chunks <= 1 ? attn_fwd_kernel<DT, 4>
                         : chunks == 2 ? attn_fwd_kernel<DT, 8>
                                       : chunks == 3 ? attn_fwd_kernel<DT, 12> : attn_fwd_kernel<DT, 16>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return VT_ERR_CUDA;
+        if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         const long long items = static_cast<long long>(p.n_qblocks) * B * H;
         if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
