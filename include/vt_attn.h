@@ -49,6 +49,7 @@
 #ifndef VT_ATTN_H
 #define VT_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -119,6 +120,41 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3],
                          int64_t D_qk, int64_t D_v,
                          float scale, int causal, vt_dtype dtype,
                          const vt_attn_opts *opts, vt_stream_t stream);
+
+/*
+ * Split-KV forward: the same operation, with the key range of every query block cut into
+ * n_split contiguous shares that separate CTAs process at the same time.  Each share writes an
+ * unnormalised partial output with its row max and row sum to `workspace`; a merge kernel then
+ * combines the shares of each row into O (the continuation step of the VeriTile coverage table's
+ * attention_fwd_triton3 row, case 4, which reads a previous M, L and Out and merges further keys).
+ * It pays off when B * H * ceil(S_q / 256) is below the number of SMs (long keys, few queries).
+ *
+ *   n_split          1 .. 64; 1 is the plain forward (workspace unused, may be NULL).
+ *   workspace        DEVICE memory owned by the caller, 256-byte aligned, at least
+ *                    vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) bytes, not overlapping
+ *                    Q, K, V or O.  Its contents are scratch: overwritten by every call, and two
+ *                    calls that share a workspace must not overlap on the GPU.
+ * bf16 I/O only for n_split > 1 (fp32 I/O returns VT_ERR_UNSUPPORTED).  Other arguments and
+ * errors as for vt_attn_fwd_strided; a too small or NULL workspace is VT_ERR_INVALID_ARG.
+ */
+vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3],
+                              const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3],
+                              void *O, const int64_t o_stride[3],
+                              int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                              int64_t D_qk, int64_t D_v,
+                              float scale, int causal, vt_dtype dtype,
+                              int n_split, void *workspace, size_t workspace_bytes,
+                              vt_stream_t stream);
+
+/* Bytes of workspace vt_attn_fwd_splitkv needs (0 when n_split <= 1 or an extent is not positive).
+ * Host-only arithmetic: no GPU call. */
+size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split);
+
+/* The number of shares this library would pick on the current device: the most that still fit
+ * one wave of CTAs with at least four 128-key tiles each; 1 when splitting does not pay (or for
+ * fp32 I/O).  Queries the current device's SM count. */
+int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char *vt_status_str(vt_status status);

@@ -22,7 +22,8 @@ STATUS = {
 }
 
 # Every symbol the header declares.
-EXPORTS = ("vt_attn_fwd", "vt_attn_fwd_strided", "vt_attn_fwd_ex", "vt_status_str", "vt_last_device_status")
+EXPORTS = ("vt_attn_fwd", "vt_attn_fwd_strided", "vt_attn_fwd_ex", "vt_attn_fwd_splitkv",
+           "vt_attn_splitkv_workspace_size", "vt_attn_splitkv_choose", "vt_status_str", "vt_last_device_status")
 
 
 class VtError(RuntimeError):
@@ -56,6 +57,14 @@ def load(path: str | None = None):
     lib.vt_attn_fwd_ex.argtypes = [vp, st3, vp, st3, vp, st3, vp, st3, i64, i64, i64, i64, i64, i64, f, i, i,
                                    ctypes.POINTER(vt_attn_opts), vp]
     lib.vt_attn_fwd_ex.restype = i
+    sz = ctypes.c_size_t
+    lib.vt_attn_fwd_splitkv.argtypes = [vp, st3, vp, st3, vp, st3, vp, st3, i64, i64, i64, i64, i64, i64, f, i, i,
+                                        i, vp, sz, vp]
+    lib.vt_attn_fwd_splitkv.restype = i
+    lib.vt_attn_splitkv_workspace_size.argtypes = [i64, i64, i64, i64, i]
+    lib.vt_attn_splitkv_workspace_size.restype = sz
+    lib.vt_attn_splitkv_choose.argtypes = [i64, i64, i64, i64, i, i]
+    lib.vt_attn_splitkv_choose.restype = i
     lib.vt_status_str.argtypes = [i]
     lib.vt_status_str.restype = ctypes.c_char_p
     lib.vt_last_device_status.argtypes = [vp]
@@ -88,6 +97,21 @@ def vt_attn_fwd_ex(Q, q_stride, K, k_stride, V, v_stride, O, o_stride,
     return load().vt_attn_fwd_ex(Q, _stride3(q_stride), K, _stride3(k_stride), V, _stride3(v_stride),
                                  O, _stride3(o_stride), B, H, S_q, S_k, D_qk, D_v, scale, int(causal), dtype,
                                  ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def vt_attn_fwd_splitkv(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                        scale, causal, dtype, n_split, workspace, workspace_bytes, stream) -> int:
+    return load().vt_attn_fwd_splitkv(Q, _stride3(q_stride), K, _stride3(k_stride), V, _stride3(v_stride),
+                                      O, _stride3(o_stride), B, H, S_q, S_k, D_qk, D_v, scale, int(causal), dtype,
+                                      int(n_split), workspace, int(workspace_bytes), stream)
+
+
+def vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) -> int:
+    return int(load().vt_attn_splitkv_workspace_size(B, H, S_q, D_v, int(n_split)))
+
+
+def vt_attn_splitkv_choose(B, H, S_q, S_k, causal, dtype) -> int:
+    return int(load().vt_attn_splitkv_choose(B, H, S_q, S_k, int(causal), dtype))
 
 
 def vt_status_str(code: int) -> str:
@@ -145,4 +169,36 @@ def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None
                         float(scale), causal, code, opts, _stream_handle(stream))
     if rc != 0:
         raise VtError(rc, "vt_attn_fwd")
+    return out
+
+
+def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, n_split: int | None = None,
+                     out=None, workspace=None, stream=None):
+    """Split-KV forward for CUDA tensors (bf16 for n_split > 1).  ``n_split=None`` uses the
+    library's choice; ``workspace`` may be a preallocated uint8 CUDA tensor of at least
+    ``vt_attn_splitkv_workspace_size`` bytes (allocated here otherwise)."""
+    import torch
+    B, H, S_q, D_qk = q.shape
+    S_k, D_v = k.shape[2], v.shape[3]
+    if k.shape != (B, H, S_k, D_qk) or v.shape != (B, H, S_k, D_v):
+        raise ValueError("shape mismatch between q, k and v")
+    code = _dtype_code(q)
+    if _dtype_code(k) != code or _dtype_code(v) != code:
+        raise TypeError("q, k and v must share one dtype")
+    if scale is None:
+        scale = float(D_qk) ** -0.5
+    if n_split is None:
+        n_split = vt_attn_splitkv_choose(B, H, S_q, S_k, causal, code)
+    if out is None:
+        out = torch.empty((B, H, S_q, D_v), dtype=q.dtype, device=q.device)
+    need = vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = vt_attn_fwd_splitkv(q.data_ptr(), _bhs_strides(q), k.data_ptr(), _bhs_strides(k), v.data_ptr(),
+                             _bhs_strides(v), out.data_ptr(), _bhs_strides(out), B, H, S_q, S_k, D_qk, D_v,
+                             float(scale), causal, code, n_split, ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise VtError(rc, "vt_attn_fwd_splitkv")
     return out

@@ -10,7 +10,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libvt_attn.so")
 SOURCES = [os.path.join(CSRC, "vt_attn_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vt_attn_kernel.cuh", "vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vt_attn_kernel.cuh", "vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_attn_merge.cuh",
+                                                  "vt_ptx.cuh")] + [
     os.path.join(os.path.dirname(PKG), "include", "vt_attn.h")]
 
 NVCC_FLAGS = [

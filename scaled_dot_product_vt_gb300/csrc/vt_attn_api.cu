@@ -14,6 +14,7 @@
 #include "../../include/vt_attn.h"
 #include "vt_attn_bf16_2q.cuh"
 #include "vt_attn_kernel.cuh"
+#include "vt_attn_merge.cuh"
 
 namespace vt {
 
@@ -128,10 +129,26 @@ bool make_map(CUtensorMap *map, const void *ptr, const int64_t st[3], int64_t B,
     return r == CUDA_SUCCESS;
 }
 
+// Workspace of a split-KV call: partial outputs, then row maxima, then row sums (256-byte aligned).
+struct SplitLayout {
+    size_t o_off, m_off, l_off, bytes;
+};
+SplitLayout split_layout(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = static_cast<size_t>(B) * H * S_q;
+    SplitLayout L;
+    L.o_off = 0;
+    L.m_off = up(static_cast<size_t>(n_split) * rows * D_v * sizeof(float));
+    L.l_off = L.m_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
+    L.bytes = L.l_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
+    return L;
+}
+
 template <int DT>
 vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
                  const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
-                 int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, cudaStream_t stream) {
+                 int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, int n_split,
+                 void *workspace, cudaStream_t stream) {
     using C = Cfg<DT>;
     CUtensorMap tq, tk, tv;
     // K/V boxes are one key tile high
@@ -166,6 +183,14 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     p.v_sb = vs[0];
     p.v_sh = vs[1];
     p.v_ss = vs[2];
+    p.n_split = n_split;
+    if (n_split > 1) {
+        const SplitLayout L = split_layout(B, H, S_q, D_v, n_split);
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        p.part_o = reinterpret_cast<float *>(ws + L.o_off);
+        p.part_m = reinterpret_cast<float *>(ws + L.m_off);
+        p.part_l = reinterpret_cast<float *>(ws + L.l_off);
+    }
     p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     p.flags = opts ? opts->flags : 0u;
 
@@ -190,7 +215,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
         const long long bh = B * H;
         long long grp = (2LL * sms + p.n_qblocks - 1) / p.n_qblocks;
         p.head_group = static_cast<int>(grp < 1 ? 1 : (grp > bh ? bh : grp));
-        const long long items = static_cast<long long>(p.n_qblocks) * bh;
+        const long long items = static_cast<long long>(p.n_qblocks) * bh * n_split;
         if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         // Q K^T K-steps of 16, rounded up to an even count (the TMA zero-fills past D_qk)
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
@@ -201,6 +226,25 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<static_cast<unsigned>(items), q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+        if (n_split > 1) {
+            MergeParams mp{};
+            mp.part_o = p.part_o;
+            mp.part_m = p.part_m;
+            mp.part_l = p.part_l;
+            mp.O = O;
+            mp.rows = B * H * S_q;
+            mp.H = static_cast<int>(H);
+            mp.S_q = static_cast<int>(S_q);
+            mp.D_v = static_cast<int>(D_v);
+            mp.n_split = n_split;
+            mp.o_sb = os[0];
+            mp.o_sh = os[1];
+            mp.o_ss = os[2];
+            const long long blocks = (mp.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock;
+            if (blocks > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+            attn_merge_kernel<2><<<static_cast<unsigned>(blocks), 32 * kMergeRowsPerBlock, 0, stream>>>(mp);
+            if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+        }
         return VT_OK;
     } else {
         // one 128-row query tile per CTA (fp32 I/O on the TF32 path)
@@ -219,6 +263,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
                         : chunks == 2 ? attn_fwd_kernel<DT, 8>
                                       : chunks == 3 ? attn_fwd_kernel<DT, 12> : attn_fwd_kernel<DT, 16>;
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
+        p.n_split = 1;  // split-KV is served by the bf16 kernel only
         const long long items = static_cast<long long>(p.n_qblocks) * B * H;
         if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
@@ -260,10 +305,18 @@ const char *vt_status_str(vt_status s) {
 
 vt_status vt_last_device_status(vt_stream_t stream) { return vt::read_status(reinterpret_cast<cudaStream_t>(stream)); }
 
-vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
-                         const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
-                         int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
-                         vt_dtype dtype, const vt_attn_opts *opts, vt_stream_t stream) {
+}  // extern "C"
+
+namespace vt {
+namespace {
+
+// Argument checks shared by every forward entry point (see include/vt_attn.h); VT_OK with
+// *empty = true for a valid empty problem.
+vt_status check_args(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                     const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
+                     int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, vt_dtype dtype,
+                     bool *empty) {
+    *empty = false;
     if (dtype != VT_F32 && dtype != VT_BF16) return VT_ERR_INVALID_ARG;
     if (B < 0 || H < 0 || S_q < 0 || S_k < 0 || D_qk < 0 || D_v < 0) return VT_ERR_INVALID_ARG;
     if (S_k == 0 || D_qk == 0 || D_v == 0) return VT_ERR_INVALID_ARG;
@@ -271,7 +324,10 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K
     if (D_qk > vt::kMaxD || D_v > vt::kMaxD) return VT_ERR_UNSUPPORTED;
     if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxExtent || S_k > vt::kMaxExtent)
         return VT_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || S_q == 0) return VT_OK;
+    if (B == 0 || H == 0 || S_q == 0) {
+        *empty = true;
+        return VT_OK;
+    }
     if (!Q || !K || !V || !O || !q_stride || !k_stride || !v_stride || !o_stride) return VT_ERR_INVALID_ARG;
     const int elt = dtype == VT_BF16 ? 2 : 4;
     const int64_t *st[4] = {q_stride, k_stride, v_stride, o_stride};
@@ -289,15 +345,88 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K
         vt::overlap(so, vt::span_of(K, k_stride, B, H, S_k, D_qk, elt)) ||
         vt::overlap(so, vt::span_of(V, v_stride, B, H, S_k, D_v, elt)))
         return VT_ERR_INVALID_ARG;
+    return VT_OK;
+}
 
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+vt_status forward(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
+                  const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                  int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype, const vt_attn_opts *opts,
+                  int n_split, void *workspace, cudaStream_t s) {
     const vt_status r = dtype == VT_BF16
-                            ? vt::launch<vt::kBF16>(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k,
-                                                    D_qk, D_v, scale, causal, opts, s)
-                            : vt::launch<vt::kF32>(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k,
-                                                   D_qk, D_v, scale, causal, opts, s);
+                            ? launch<kBF16>(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, opts,
+                                            n_split, workspace, s)
+                            : launch<kF32>(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, opts,
+                                           n_split, workspace, s);
     if (r != VT_OK) return r;
-    return vt::env_check() ? vt::read_status(s) : VT_OK;
+    return env_check() ? read_status(s) : VT_OK;
+}
+
+}  // namespace
+}  // namespace vt
+
+extern "C" {
+
+vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                         const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
+                         int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
+                         vt_dtype dtype, const vt_attn_opts *opts, vt_stream_t stream) {
+    bool empty = false;
+    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                                       scale, dtype, &empty);
+    if (c != VT_OK || empty) return c;
+    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
+                       dtype, opts, 1, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split) {
+    if (B <= 0 || H <= 0 || S_q <= 0 || D_v <= 0 || n_split <= 1) return 0;
+    return vt::split_layout(B, H, S_q, D_v, n_split).bytes;
+}
+
+int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype) {
+    (void)causal;
+    if (dtype != VT_BF16 || B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    // Shares only pay when every CTA still fits in one wave, and each share keeps >= 4 key tiles.
+    const long long items = B * H * ((S_q + vt::q2::kRows - 1) / vt::q2::kRows);
+    const long long tiles = (S_k + vt::q2::kBN - 1) / vt::q2::kBN;
+    long long n = items >= sms ? 1 : sms / items;
+    if (n > tiles / 4) n = tiles / 4;
+    if (n > vt::kMaxSplit) n = vt::kMaxSplit;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
+vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
+                              int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
+                              vt_dtype dtype, int n_split, void *workspace, size_t workspace_bytes,
+                              vt_stream_t stream) {
+    bool empty = false;
+    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                                       scale, dtype, &empty);
+    if (c != VT_OK) return c;
+    if (n_split < 1) return VT_ERR_INVALID_ARG;
+    if (n_split > vt::kMaxSplit) return VT_ERR_UNSUPPORTED;
+    if (empty) return VT_OK;
+    if (n_split > 1) {
+        if (dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
+        if (!workspace || workspace_bytes < vt::split_layout(B, H, S_q, D_v, n_split).bytes)
+            return VT_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(workspace) % 256) return VT_ERR_MISALIGNED;
+        // the partial outputs must not overlap any tensor of the call
+        const vt::Span w{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + workspace_bytes};
+        const int elt = 2;
+        if (vt::overlap(w, vt::span_of(Q, q_stride, B, H, S_q, D_qk, elt)) ||
+            vt::overlap(w, vt::span_of(K, k_stride, B, H, S_k, D_qk, elt)) ||
+            vt::overlap(w, vt::span_of(V, v_stride, B, H, S_k, D_v, elt)) ||
+            vt::overlap(w, vt::span_of(O, o_stride, B, H, S_q, D_v, elt)))
+            return VT_ERR_INVALID_ARG;
+    }
+    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
+                       dtype, nullptr, n_split, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],

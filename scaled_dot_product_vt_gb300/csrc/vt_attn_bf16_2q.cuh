@@ -85,11 +85,14 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work item: groups of `head_group` heads; inside a group, heavy causal blocks first
+    // ---- work item: groups of `head_group` heads; inside a group, heavy causal blocks first;
+    // the splits of one item are adjacent in the launch order
+    const int split = blockIdx.x % p.n_split;
+    const int item = blockIdx.x / p.n_split;
     const int BH = p.B * p.H;
     const int per_group = p.head_group * p.n_qblocks;
-    const int g = blockIdx.x / per_group;
-    const int rr = blockIdx.x - g * per_group;
+    const int g = item / per_group;
+    const int rr = item - g * per_group;
     const int g_heads = min(p.head_group, BH - g * p.head_group);
     const int slot_q = rr / g_heads;
     const int bh = g * p.head_group + (rr - slot_q * g_heads);
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 
     // key tiles each query tile needs (0 when the tile lies past S_q)
     const int n_all = (p.S_k + BN - 1) / BN;
-    int n0, n1;
+    int n0, n1, j0;
     {
         int n[2];
 #pragma unroll
@@ -110,8 +113,13 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             else if (p.causal) n[t] = min(n_all, (min(first + kBM, p.S_q) - 1) / BN + 1);
             else n[t] = n_all;
         }
-        n0 = n[0];
-        n1 = n[1];
+        // this CTA's contiguous share of the item's key tiles: [j0, j_end)
+        const int n_item = max(n[0], n[1]);
+        const int per = (n_item + p.n_split - 1) / p.n_split;
+        const int lo = min(split * per, n_item), hi = min(n_item, lo + per);
+        n0 = max(0, min(n[0], hi) - lo);  // key tiles of this share each query tile needs
+        n1 = max(0, min(n[1], hi) - lo);
+        j0 = lo;
     }
     const int n_kv = max(n0, n1);
     const int n_slots = p.stages;
@@ -160,7 +168,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && n_kv > 0) {
             const int q_tiles = n1 > 0 ? 2 : 1;
             mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_tiles * q_tile_bytes);
             for (int c = 0; c < p.q_chunks; ++c)
@@ -185,11 +193,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 if ((i & 1) == 0) {
                     mbar_arrive_expect_tx(bar, k_bytes);
                     for (int c = 0; c < p.q_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, j * BN, h, b);
+                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, (j0 + j) * BN, h, b);
                 } else {
                     mbar_arrive_expect_tx(bar, v_bytes);
                     for (int c = 0; c < p.v_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, j * BN, h, b);
+                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, (j0 + j) * BN, h, b);
                 }
                 ++loads;
                 if (++s == n_slots) s = 0;
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && n_kv > 0) {
             const uint32_t idesc_qk = instr_desc(1, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(1, kBM, p.n_pv, 1);
             // Descriptors as (low, high) words: offsets only move the low word (start address >> 4).
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
             }
-            const int k0 = j * BN;
+            const int k0 = (j0 + j) * BN;
             if ((k0 + BN > p.S_k) || (p.causal && k0 + BN - 1 > tile_row0)) {
                 const int lim = p.causal ? min(p.S_k, q_row + 1) : p.S_k;  // keys k0+k < lim are allowed
 #pragma unroll
@@ -405,34 +413,68 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         if (ok && n_my > 0) {
             ok = wait_bounded(smem_u32(&ctl.o_done[t]), 0, ctl.abort_flag, p);
             ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                // ------------------------------------------------------------ epilogue
-                tc_fence_after();
-                const float inv_l = 1.0f / l;
-                const bool row_ok = q_row < p.S_q;
-                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                                (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
-                                 static_cast<long long>(q_row) * p.o_ss) * 2;
-                for (int cc = 0; cc < p.n_pv; cc += 16) {
-                    uint32_t o[16];
+        }
+        const bool row_ok = q_row < p.S_q;
+        if (ok && n_my > 0 && p.n_split == 1) {
+            // ------------------------------------------------------------ epilogue: O = O_t / l
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                            (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
+                             static_cast<long long>(q_row) * p.o_ss) * 2;
+            for (int cc = 0; cc < p.n_pv; cc += 16) {
+                uint32_t o[16];
+                tmem_ld16(o_addr + cc, o);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                if (cc + 16 <= p.D_v) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+                    uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                }
+            }
+        } else if (ok && p.n_split > 1) {
+            // ------------------------------------------------------------ epilogue: partial O, m, l
+            // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
+            // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
+            const long long row_lin = (static_cast<long long>(b) * p.H + h) * p.S_q + q_row;
+            const long long part = static_cast<long long>(split) * p.B * p.H * p.S_q + row_lin;
+            float *orow = p.part_o + part * p.D_v;
+            if (n_my > 0) tc_fence_after();
+            for (int cc = 0; cc < p.n_pv; cc += 16) {
+                uint32_t o[16];
+                if (n_my > 0) {
                     tmem_ld16(o_addr + cc, o);
                     tmem_wait_ld();
-                    if (!row_ok) continue;
-                    uint32_t w[8];
+                } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-                    if (cc + 16 <= p.D_v) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    } else {
-                        uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
-                    }
+                    for (int k = 0; k < 16; ++k) o[k] = 0u;
                 }
+                if (!row_ok) continue;
+                if (cc + 16 <= p.D_v) {
+                    float4 *dst = reinterpret_cast<float4 *>(orow + cc);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                             __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (cc + k < p.D_v) orow[cc + k] = __uint_as_float(o[k]);
+                }
+            }
+            if (row_ok) {
+                p.part_m[part] = n_my > 0 ? m_used : -INFINITY;
+                p.part_l[part] = n_my > 0 ? l : 0.0f;
             }
         }
     }

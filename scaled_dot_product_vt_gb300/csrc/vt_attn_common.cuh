@@ -11,6 +11,7 @@ namespace vt {
 
 constexpr int kBM = 128;           // query rows per work item (= TMEM lanes)
 constexpr int kMaxStages = 4;
+constexpr int kMaxSplit = 64;       // split-KV shares per work item, at most
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
 
 // Device status bits (the host maps them to vt_status codes).
@@ -34,6 +35,13 @@ struct AttnParams {
     long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
     const void *V;               // read by the fp32 V loader
     long long v_sb, v_sh, v_ss;
+    // Split-KV: each work item's key tiles are cut into n_split contiguous ranges, one per CTA; with
+    // n_split > 1 the CTAs write unnormalised partial outputs (fp32, D_v per row), their row max m
+    // (log2 units, -inf if no allowed key) and row sum l, indexed [split][(b*H + h)*S_q + i].
+    int n_split;
+    float *part_o;
+    float *part_m;
+    float *part_l;
     unsigned long long timeout_ns;
     unsigned flags;
     unsigned *status;  // device status word

@@ -1,0 +1,70 @@
+// Split-KV merge: combine the per-share partial outputs of one query row into O.
+//
+// Share s of row r holds an unnormalised output O_s (fp32, D_v values), its reference max m_s
+// (log2 units; -inf when the share had no allowed key) and its sum l_s, all relative to m_s.  In
+// real arithmetic O[r] = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s for any M; M = max_s m_s
+// keeps every weight <= 1.  This is the continuation step of the coverage table's
+// attention_fwd_triton3 row (case 4 reads M, L and Out and merges a further key range), applied
+// to all shares at once.  HBM-bound: per row it reads n_split * (D_v + 2) floats and writes D_v.
+#pragma once
+
+#include <cstdint>
+
+#include "vt_ptx.cuh"
+
+namespace vt {
+
+struct MergeParams {
+    const float *part_o;
+    const float *part_m;
+    const float *part_l;
+    void *O;
+    long long rows;  // B * H * S_q
+    int H, S_q, D_v, n_split;
+    long long o_sb, o_sh, o_ss;
+};
+
+constexpr int kMergeRowsPerBlock = 4;  // one warp per row
+
+// ELT: 2 = bf16 output, 4 = fp32 output.  D_v <= 128: lane L handles columns L, L+32, L+64, L+96.
+template <int ELT>
+__global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
+    attn_merge_kernel(const MergeParams mp) {
+    const int lane = threadIdx.x & 31;
+    const long long row = static_cast<long long>(blockIdx.x) * kMergeRowsPerBlock + (threadIdx.x >> 5);
+    if (row >= mp.rows) return;
+    float M = -INFINITY;
+    for (int s = 0; s < mp.n_split; ++s) M = fmaxf(M, mp.part_m[s * mp.rows + row]);
+    float L = 0.0f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < mp.n_split; ++s) {
+        const float ms = mp.part_m[s * mp.rows + row];
+        if (ms == -INFINITY) continue;  // no allowed key in this share
+        const float w = ex2(ms - M);
+        L += w * mp.part_l[s * mp.rows + row];
+        const float *po = mp.part_o + (s * mp.rows + row) * mp.D_v;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int col = lane + 32 * c;
+            if (col < mp.D_v) acc[c] += w * po[col];
+        }
+    }
+    const float inv = 1.0f / L;
+    const long long i = row % mp.S_q;
+    const long long bh = row / mp.S_q;
+    const long long h = bh % mp.H, b = bh / mp.H;
+    uint8_t *orow = reinterpret_cast<uint8_t *>(mp.O) + (b * mp.o_sb + h * mp.o_sh + i * mp.o_ss) * ELT;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int col = lane + 32 * c;
+        if (col >= mp.D_v) continue;
+        const float v = acc[c] * inv;
+        if (ELT == 2) {
+            reinterpret_cast<uint16_t *>(orow)[col] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+        } else {
+            reinterpret_cast<float *>(orow)[col] = v;
+        }
+    }
+}
+
+}  // namespace vt

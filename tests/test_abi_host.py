@@ -90,3 +90,42 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no fallback"):
         vt.load(str(tmp_path / "libvt_attn.so"))
+
+
+# ---------------------------------------------------------------- split-KV entry points
+
+def test_splitkv_workspace_size(lib):
+    assert vt.vt_attn_splitkv_workspace_size(2, 3, 5, 8, 1) == 0
+    assert vt.vt_attn_splitkv_workspace_size(2, 3, 5, 8, 0) == 0
+    assert vt.vt_attn_splitkv_workspace_size(0, 3, 5, 8, 4) == 0
+    up = lambda x: (x + 255) // 256 * 256
+    rows = 2 * 3 * 5
+    expect = up(4 * rows * 8 * 4) + 2 * up(4 * rows * 4)
+    assert vt.vt_attn_splitkv_workspace_size(2, 3, 5, 8, 4) == expect
+
+
+def split_call(n_split=2, dtype=vt.VT_BF16, ws=8 * A, ws_bytes=1 << 24, D_v=8):
+    st = (32, 32, 8)
+    so = (32, 32, D_v)
+    return vt.vt_attn_fwd_splitkv(A, st, 2 * A, st, 3 * A, (32, 32, D_v), 4 * A, so, 1, 1, 4, 4, 8, D_v,
+                                  0.5, 0, dtype, n_split, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_split=0), 1), (dict(n_split=-3), 1), (dict(n_split=65), 2),
+    (dict(dtype=vt.VT_F32), 2),                       # split-KV serves bf16 only
+    (dict(ws=None), 1), (dict(ws_bytes=64), 1),       # missing or too small workspace
+    (dict(ws=8 * A + 16), 3),                         # workspace not 256-byte aligned
+    (dict(ws=A), 1),                                  # workspace overlaps Q
+])
+def test_splitkv_argument_errors(lib, kw, code):
+    assert split_call(**kw) == code
+
+
+def test_splitkv_choose_without_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    # no device to query: falls back to no split
+    assert vt.vt_attn_splitkv_choose(1, 8, 256, 32768, 0, vt.VT_BF16) == 1
+    assert vt.vt_attn_splitkv_choose(1, 8, 256, 32768, 0, vt.VT_F32) == 1
