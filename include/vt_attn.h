@@ -156,6 +156,36 @@ size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
  * fp32 I/O).  Queries the current device's SM count. */
 int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype);
 
+/*
+ * vt_attn_fwd_splitkv without a caller-provided workspace, for callers that cannot allocate
+ * device memory: for example a plugin running inside a host framework that owns every byte of
+ * device memory and does not let extensions call cudaMalloc, or a latency-critical service that
+ * must not allocate after start-up because an allocation can block and synchronise the device.
+ * The pages describe no such call; it has no counterpart in them.
+ *
+ * The shares' partial results live in a fixed 32 MiB array inside this library (a static
+ * __device__ array: every GPU that loads the library holds it until the process exits).  The call
+ * itself allocates nothing.  Arguments and errors are those of vt_attn_fwd_splitkv without the
+ * workspace; in addition, a problem whose partial results need more than 32 MiB
+ * (vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) > 33554432) is rejected with
+ * VT_ERR_UNSUPPORTED before anything runs.  n_split = 1 uses no scratch at all.
+ *
+ * The first call with n_split > 1 on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and remembers it; make that first call before any stream capture.  All
+ * calls share the one array, which keeps whatever the last call left there: every call writes all
+ * the partial results it reads, so nothing has to start at zero, but calls that overlap on the GPU
+ * (concurrent streams, or several host threads) race on the array and must be serialised by the
+ * caller.
+ */
+vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3],
+                                      const void *K, const int64_t k_stride[3],
+                                      const void *V, const int64_t v_stride[3],
+                                      void *O, const int64_t o_stride[3],
+                                      int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                                      int64_t D_qk, int64_t D_v,
+                                      float scale, int causal, vt_dtype dtype,
+                                      int n_split, vt_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *vt_status_str(vt_status status);
 

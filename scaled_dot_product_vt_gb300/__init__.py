@@ -23,7 +23,8 @@ STATUS = {
 
 # Every symbol the header declares.
 EXPORTS = ("vt_attn_fwd", "vt_attn_fwd_strided", "vt_attn_fwd_ex", "vt_attn_fwd_splitkv",
-           "vt_attn_splitkv_workspace_size", "vt_attn_splitkv_choose", "vt_status_str", "vt_last_device_status")
+           "vt_attn_splitkv_workspace_size", "vt_attn_splitkv_choose", "vt_attn_fwd_splitkv_noalloc",
+           "vt_status_str", "vt_last_device_status")
 
 
 class VtError(RuntimeError):
@@ -65,6 +66,9 @@ def load(path: str | None = None):
     lib.vt_attn_splitkv_workspace_size.restype = sz
     lib.vt_attn_splitkv_choose.argtypes = [i64, i64, i64, i64, i, i]
     lib.vt_attn_splitkv_choose.restype = i
+    lib.vt_attn_fwd_splitkv_noalloc.argtypes = [vp, st3, vp, st3, vp, st3, vp, st3, i64, i64, i64, i64, i64, i64,
+                                                f, i, i, i, vp]
+    lib.vt_attn_fwd_splitkv_noalloc.restype = i
     lib.vt_status_str.argtypes = [i]
     lib.vt_status_str.restype = ctypes.c_char_p
     lib.vt_last_device_status.argtypes = [vp]
@@ -112,6 +116,15 @@ def vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) -> int:
 
 def vt_attn_splitkv_choose(B, H, S_q, S_k, causal, dtype) -> int:
     return int(load().vt_attn_splitkv_choose(B, H, S_q, S_k, int(causal), dtype))
+
+
+def vt_attn_fwd_splitkv_noalloc(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                                scale, causal, dtype, n_split, stream) -> int:
+    """Split-KV forward whose scratch is the library's fixed 32 MiB device array: for callers that
+    may not allocate device memory.  Raw device addresses (ints); returns the vt_status code."""
+    return load().vt_attn_fwd_splitkv_noalloc(Q, _stride3(q_stride), K, _stride3(k_stride), V, _stride3(v_stride),
+                                              O, _stride3(o_stride), B, H, S_q, S_k, D_qk, D_v, scale, int(causal),
+                                              dtype, int(n_split), stream)
 
 
 def vt_status_str(code: int) -> str:

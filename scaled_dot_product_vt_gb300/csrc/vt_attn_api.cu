@@ -20,6 +20,11 @@ namespace vt {
 
 __device__ unsigned g_status_word;  // device status bits (kStatusTimeout, kStatusBounds)
 
+// Scratch of vt_attn_fwd_splitkv_noalloc, for callers that cannot allocate device memory: a
+// fixed array that exists on every GPU that loads this library, for as long as the process runs.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int64_t kMaxD = 128;
@@ -272,6 +277,21 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     }
 }
 
+// Device address of g_noalloc_scratch on the current device (nullptr on failure).  The host-side
+// name of the array is only a stand-in, so the address is looked up with cudaGetSymbolAddress,
+// once per device with that device current, and remembered.
+void *noalloc_scratch(int dev) {
+    static void *addr[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_info_mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
 vt_status read_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return VT_ERR_CUDA;
     unsigned w = 0;
@@ -427,6 +447,32 @@ vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3], const vo
     }
     return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
                        dtype, nullptr, n_split, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], const void *K,
+                                      const int64_t k_stride[3], const void *V, const int64_t v_stride[3], void *O,
+                                      const int64_t o_stride[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
+                                      int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype, int n_split,
+                                      vt_stream_t stream) {
+    bool empty = false;
+    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                                       scale, dtype, &empty);
+    if (c != VT_OK) return c;
+    if (n_split < 1) return VT_ERR_INVALID_ARG;
+    if (n_split > vt::kMaxSplit) return VT_ERR_UNSUPPORTED;
+    if (empty) return VT_OK;
+    void *scratch = nullptr;
+    if (n_split > 1) {
+        if (dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
+        // The shares' partial results must fit the fixed array; nothing is allocated instead.
+        if (vt::split_layout(B, H, S_q, D_v, n_split).bytes > vt::kNoAllocScratchBytes) return VT_ERR_UNSUPPORTED;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return VT_ERR_CUDA;
+        scratch = vt::noalloc_scratch(dev);
+        if (!scratch) return VT_ERR_CUDA;
+    }
+    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
+                       dtype, nullptr, n_split, scratch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
