@@ -32,6 +32,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 F32, BF16 = 0, 1
+MASKS = {"none": 0, "causal": 1, "window": 2, "window_complement": 3}
 
 
 def build(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
@@ -62,6 +63,11 @@ def load(path: str | None = None):
     lib.oracle_attn_rows.restype = i
     lib.oracle_attn_fwd_ld.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, d, i, i]
     lib.oracle_attn_fwd_ld.restype = i
+    lib.oracle_attn_general.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, d, i, i64, i64, i,
+                                        vp, i64, i]
+    lib.oracle_attn_general.restype = i
+    lib.oracle_attn_general_ld.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, d, i, i64, i64, i]
+    lib.oracle_attn_general_ld.restype = i
     if path == _LIB:
         _lib = lib
     return lib
@@ -131,3 +137,61 @@ def attn_fwd_longdouble(Q, K, V, scale: float, causal: bool, lib=None) -> np.nda
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd_ld failed with code {rc}")
     return O
+
+
+def _prep_general(Q, K, V):
+    Q, K, V = (np.ascontiguousarray(x) for x in (Q, K, V))
+    code = _dtype_code(Q)
+    if _dtype_code(K) != code or _dtype_code(V) != code:
+        raise TypeError("Q, K and V must share one dtype")
+    B, H, S_q, D_qk = Q.shape
+    B2, H_kv, S_k, D_qk2 = K.shape
+    B3, H_kv3, S_k3, D_v = V.shape
+    if (B, D_qk) != (B2, D_qk2) or (B, H_kv, S_k) != (B3, H_kv3, S_k3):
+        raise ValueError("shape mismatch between Q, K and V")
+    return Q, K, V, code, (B, H, H_kv, S_q, S_k, D_qk, D_v)
+
+
+def attn_general(Q, K, V, scale: float, mask: str = "none", offset: int = 0, window: int = 0, rows=None,
+                 with_lse: bool = False, nthreads: int | None = None, lib=None):
+    """General form: Q [B,H,S_q,D_qk], K [B,H_kv,S_k,D_qk], V [B,H_kv,S_k,D_v] (H a multiple of H_kv).
+
+    ``mask`` is one of ``MASKS``; ``offset`` >= 0 and ``window`` >= 1 as in attn_oracle.c.  Returns
+    O (float64, [B,H,S_q,D_v], or (n, D_v) for ``rows`` = (n, 3) triples (b, h, i)), and with
+    ``with_lse`` also the natural-log LSE per row ([B,H,S_q] or (n,)).
+    """
+    lib = lib or load()
+    Q, K, V, code, (B, H, H_kv, S_q, S_k, D_qk, D_v) = _prep_general(Q, K, V)
+    if rows is None:
+        O = np.empty((B, H, S_q, D_v), dtype=np.float64)
+        L = np.empty((B, H, S_q), dtype=np.float64) if with_lse else None
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        O = np.empty((rows.shape[0], D_v), dtype=np.float64)
+        L = np.empty((rows.shape[0],), dtype=np.float64) if with_lse else None
+        rp, nr = rows.ctypes.data, rows.shape[0]
+    rc = lib.oracle_attn_general(Q.ctypes.data, K.ctypes.data, V.ctypes.data, O.ctypes.data,
+                                 L.ctypes.data if L is not None else None, B, H, H_kv, S_q, S_k, D_qk, D_v,
+                                 float(np.float32(scale)), MASKS[mask], int(offset), int(window), code, rp, nr,
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_attn_general failed with code {rc}")
+    return (O, L) if with_lse else O
+
+
+def attn_general_longdouble(Q, K, V, scale: float, mask: str = "none", offset: int = 0, window: int = 0,
+                            lib=None):
+    """Long-double brute force of the general form (tiny inputs): returns (O, LSE) as numpy longdouble."""
+    lib = lib or load()
+    Q, K, V, code, (B, H, H_kv, S_q, S_k, D_qk, D_v) = _prep_general(Q, K, V)
+    O = np.empty((B, H, S_q, D_v), dtype=np.longdouble)
+    L = np.empty((B, H, S_q), dtype=np.longdouble)
+    if ctypes.sizeof(ctypes.c_longdouble) != O.itemsize:
+        raise RuntimeError("numpy longdouble does not match C long double on this host")
+    rc = lib.oracle_attn_general_ld(Q.ctypes.data, K.ctypes.data, V.ctypes.data, O.ctypes.data, L.ctypes.data,
+                                    B, H, H_kv, S_q, S_k, D_qk, D_v, float(np.float32(scale)), MASKS[mask],
+                                    int(offset), int(window), code)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_general_ld failed with code {rc}")
+    return O, L

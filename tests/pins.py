@@ -4,7 +4,11 @@ Each pin takes a loaded oracle library (the real one, or a deliberately broken
 copy built by the mutation test) and raises AssertionError when the fact fails.
 The definition pinned is the naive reference of the VeriTile page
 "VeriTile.Examples.FlashAttention1.NaiveRefinement" (fa1NaiveReference4D and the
-causal form, key j <= query i) and the accy page's CPU routine `expectedOutput`.
+causal form, key j <= query i) and the accy page's CPU routine `expectedOutput`;
+the general form's extras (grouped key/value heads, the offset causal mask, the
+sliding window and its complement, the per-row log-sum-exp) are pinned against
+the plain non-causal definition on truncated or repeated inputs and against
+closed forms.
 """
 
 from __future__ import annotations
@@ -275,11 +279,165 @@ def pin_shape_convention():
     assert element_counts(3, 1, 2, 4, 5, 3) == (30, 60, 36, 18)
 
 
+# ---- the general form: grouped heads, offset causal, windows, log-sum-exp ---------------------
+
+def _G(lib, Q, K, V, scale, mask="none", offset=0, window=0, lse=False):
+    return oracle.attn_general(Q, K, V, scale, mask, offset, window, with_lse=lse, nthreads=2, lib=lib)
+
+
+def _plain_rows(lib, Q, K, V, scale, i, lo, hi):
+    """Non-causal softmax of query row i over keys lo..hi (inclusive), every (b, h)."""
+    return _O(lib, Q[:, :, i:i + 1], K[:, :, lo:hi + 1], V[:, :, lo:hi + 1], scale, False)
+
+
+def pin_offset_causal_prefix(lib):
+    """Offset causal: query i at key position i + o sees keys 0..min(i + o, S_k - 1).
+
+    The VeriTile coverage table's attention_llama causal row gives query block p the key span
+    (p + 1) BLOCK_N + start_position: query i reaches key i + start_position.  o = S_k - S_q is
+    the bottom-right alignment (the last query sees every key); o >= S_k - 1 allows every key.
+    """
+    S_q, S_k = 5, 9
+    Q, K, V = _rand((1, 2, S_q, 4), 40), _rand((1, 2, S_k, 4), 41), _rand((1, 2, S_k, 3), 42)
+    for o in (0, 1, 3, S_k - S_q, 8, 20):
+        O = _G(lib, Q, K, V, 0.7, "causal", o)
+        for i in range(S_q):
+            ref = _plain_rows(lib, Q, K, V, 0.7, i, 0, min(i + o, S_k - 1))
+            assert np.allclose(O[:, :, i:i + 1], ref, atol=1e-13), f"offset {o} row {i}"
+    assert np.allclose(_G(lib, Q, K, V, 0.7, "causal", S_k - 1), _O(lib, Q, K, V, 0.7, False), atol=1e-13)
+
+
+def pin_window_recent_keys(lib):
+    """Sliding window w, offset o: row i sees keys max(0, i+o-w+1)..min(i+o, S_k-1), the w most recent.
+
+    w = 1 returns V[i + o] exactly; a row whose window lies past the last key has no key and is 0.
+    """
+    S_q, S_k = 6, 10
+    Q, K, V = _rand((1, 2, S_q, 3), 43, 2.0), _rand((1, 2, S_k, 3), 44), _rand((1, 2, S_k, 4), 45)
+    for o, w in ((0, 1), (0, 3), (2, 2), (4, 5), (3, 40), (8, 2)):
+        O = _G(lib, Q, K, V, 0.9, "window", o, w)
+        for i in range(S_q):
+            lo, hi = max(0, i + o - w + 1), min(i + o, S_k - 1)
+            if lo > hi:
+                assert np.all(O[:, :, i] == 0.0), f"window {w} offset {o}: row {i} has no key"
+                continue
+            ref = _plain_rows(lib, Q, K, V, 0.9, i, lo, hi)
+            assert np.allclose(O[:, :, i:i + 1], ref, atol=1e-13), f"window {w} offset {o} row {i}"
+            if w == 1:
+                assert np.array_equal(O[:, :, i], V[:, :, i + o].astype(np.float64))
+
+
+def pin_window_complement(lib):
+    """Complement of the window: row i sees keys 0..min(i+o-w, S_k-1); rows with i + o < w have none
+    (O = 0, LSE = -inf)."""
+    S_q, S_k = 7, 8
+    Q, K, V = _rand((2, 1, S_q, 3), 46, 2.0), _rand((2, 1, S_k, 3), 47), _rand((2, 1, S_k, 2), 48)
+    for o, w in ((0, 1), (0, 3), (1, 4), (5, 2), (0, 9)):
+        O, L = _G(lib, Q, K, V, 1.1, "window_complement", o, w, lse=True)
+        for i in range(S_q):
+            hi = min(i + o - w, S_k - 1)
+            if hi < 0:
+                assert np.all(O[:, :, i] == 0.0) and np.all(L[:, :, i] == -np.inf), f"row {i} is empty"
+                continue
+            ref = _plain_rows(lib, Q, K, V, 1.1, i, 0, hi)
+            assert np.allclose(O[:, :, i:i + 1], ref, atol=1e-13), f"complement {w} offset {o} row {i}"
+
+
+def pin_window_split_merges_to_causal(lib):
+    """Window and complement split each causal key set in two.  Merging their outputs with their
+    log-sum-exps, O = sum_k e^{LSE_k} O_k / sum_k e^{LSE_k} (the continuation case of the
+    attention_fwd_triton3 row), gives the offset causal output and LSE = log(e^{LSE_w} + e^{LSE_c})."""
+    S = 9
+    Q, K, V = _rand((1, 2, S, 4), 49, 2.0), _rand((1, 2, S + 3, 4), 50), _rand((1, 2, S + 3, 3), 51)
+    for o, w in ((0, 3), (3, 1), (2, 6), (0, 20)):
+        Ow, Lw = _G(lib, Q, K, V, 0.8, "window", o, w, lse=True)
+        Oc, Lc = _G(lib, Q, K, V, 0.8, "window_complement", o, w, lse=True)
+        M = np.maximum(Lw, Lc)
+        ww, wc = np.exp(Lw - M), np.exp(Lc - M)
+        Om = (ww[..., None] * Ow + wc[..., None] * Oc) / (ww + wc)[..., None]
+        for i in range(S):
+            ref = _plain_rows(lib, Q, K, V, 0.8, i, 0, min(i + o, S + 2))
+            assert np.allclose(Om[:, :, i:i + 1], ref, atol=1e-12), f"window {w} offset {o} row {i}"
+        Lf = np.log(np.exp(Lw - M) + np.exp(Lc - M)) + M
+        _, Lcausal = _G(lib, Q, K, V, 0.8, "causal", o, lse=True)
+        assert np.allclose(Lf, Lcausal, atol=1e-12)
+
+
+def pin_lse_closed_forms(lib):
+    """LSE_i = log sum_{j in A_i} exp(s_j): scale 0 gives log |A_i|; one key gives its score;
+    D_qk = 1, S_k = 2 gives log(e^a + e^b)."""
+    Q, K, V = _rand((1, 2, 6, 3), 52), _rand((1, 2, 6, 3), 53), _rand((1, 2, 6, 2), 54)
+    _, L = _G(lib, Q, K, V, 0.0, "none", lse=True)
+    assert np.allclose(L, math.log(6), atol=1e-14)
+    _, L = _G(lib, Q, K, V, 0.0, "causal", lse=True)
+    assert np.allclose(L, np.log(np.arange(1, 7))[None, None, :], atol=1e-14)
+    _, L = _G(lib, Q, K, V, 0.0, "window", 0, 2, lse=True)
+    assert np.allclose(L, np.log(np.minimum(np.arange(1, 7), 2))[None, None, :], atol=1e-14)
+    q = np.array([0.5, -1.25, 2.0, 0.0, 3.5], np.float32).reshape(1, 1, 5, 1)
+    k = np.array([0.75, -0.5], np.float32).reshape(1, 1, 2, 1)
+    v = np.ones((1, 1, 2, 1), np.float32)
+    _, L = _G(lib, q, k[:, :, :1], v[:, :, :1], 0.625, "none", lse=True)
+    assert np.allclose(L[0, 0], 0.625 * q[0, 0, :, 0].astype(np.float64) * 0.75, atol=1e-14)
+    _, L = _G(lib, q, k, v, 0.625, "none", lse=True)
+    a, b = 0.625 * q[0, 0, :, 0].astype(np.float64) * 0.75, 0.625 * q[0, 0, :, 0].astype(np.float64) * -0.5
+    assert np.allclose(L[0, 0], np.log(np.exp(a) + np.exp(b)), atol=1e-14)
+
+
+def pin_grouped_heads_expand(lib):
+    """H_kv < H: the result equals multi-head attention with each key/value head repeated for its
+    H / H_kv query heads (query head h reads head h // (H / H_kv)); H_kv = 1 is multi-query."""
+    Q = _rand((2, 6, 5, 4), 55)
+    for H_kv in (3, 2, 1):
+        K, V = _rand((2, H_kv, 7, 4), 56 + H_kv), _rand((2, H_kv, 7, 3), 60 + H_kv)
+        rep = 6 // H_kv
+        Kx, Vx = np.repeat(K, rep, axis=1), np.repeat(V, rep, axis=1)
+        for mask in ("none", "causal"):
+            O = _G(lib, Q, K, V, 0.6, mask)
+            assert np.allclose(O, _O(lib, Q, Kx, Vx, 0.6, mask == "causal"), atol=1e-13), f"H_kv {H_kv} {mask}"
+
+
+def pin_general_rows_match_full(lib):
+    """The general form's sampled rows equal the same rows of its full result (grouped heads, window)."""
+    Q, K, V = make_qkv(2, 4, 9, 11, 5, 4, "bf16", seed=64)
+    K, V = K[:, :2].copy(), V[:, :2].copy()
+    full, L = _G(lib, Q, K, V, 0.3, "window", 2, 4, lse=True)
+    rows = np.array([[0, 0, 0], [1, 3, 8], [0, 1, 4], [1, 2, 3]])
+    got, Lr = oracle.attn_general(Q, K, V, 0.3, "window", 2, 4, rows=rows, with_lse=True, nthreads=2, lib=lib)
+    assert np.array_equal(got, full[rows[:, 0], rows[:, 1], rows[:, 2]])
+    assert np.array_equal(Lr, L[rows[:, 0], rows[:, 1], rows[:, 2]])
+
+
+def pin_general_longdouble(lib):
+    """The general form agrees with its long-double brute force (no max shift) on random tiny cases,
+    O to 1e-12 and LSE to 1e-12 (empty rows: both 0 and -inf)."""
+    rng = np.random.default_rng(65)
+    masks = list(oracle.MASKS)
+    for t in range(24):
+        B = int(rng.integers(1, 3))
+        H_kv = int(rng.integers(1, 3))
+        H = H_kv * int(rng.integers(1, 4))
+        S_q, S_k, D_qk, D_v = (int(x) for x in rng.integers(1, 9, size=4))
+        mask = masks[t % 4]
+        offset, window = int(rng.integers(0, 6)), int(rng.integers(1, 6))
+        Q, _, _ = make_qkv(B, H, S_q, S_k, D_qk, D_v, "f32", seed=200 + t)
+        _, K, V = make_qkv(B, H_kv, S_q, S_k, D_qk, D_v, "f32", seed=300 + t)
+        scale = float(np.float32(1.0 / math.sqrt(D_qk)))
+        O, L = _G(lib, Q, K, V, scale, mask, offset, window, lse=True)
+        Ol, Ll = oracle.attn_general_longdouble(Q, K, V, scale, mask, offset, window, lib=lib)
+        assert np.abs(O - Ol.astype(np.float64)).max() <= 1e-12, f"case {t}"
+        Ll = Ll.astype(np.float64)
+        assert np.array_equal(np.isinf(L), np.isinf(Ll)), f"case {t}: empty rows"
+        fin = np.isfinite(L)
+        assert np.abs(L[fin] - Ll[fin]).max(initial=0.0) <= 1e-12, f"case {t}"
+
+
 # Pins that do not compare the oracle with its own long-double brute force.
 INDEPENDENT_PINS = [
     pin_ones_value, pin_identical_keys_mean, pin_scale_zero_mean, pin_key_permutation,
     pin_causal_row0_and_prefix, pin_single_key, pin_logistic, pin_hand_rows, pin_shift_invariance,
     pin_peaky, pin_convexity, pin_selector_unequal_dims, pin_heads_independent, pin_bf16_widening,
     pin_worked_example, pin_rows_match_full,
+    pin_offset_causal_prefix, pin_window_recent_keys, pin_window_complement, pin_window_split_merges_to_causal,
+    pin_lse_closed_forms, pin_grouped_heads_expand, pin_general_rows_match_full,
 ]
-ALL_PINS = INDEPENDENT_PINS + [pin_longdouble]
+ALL_PINS = INDEPENDENT_PINS + [pin_longdouble, pin_general_longdouble]

@@ -65,23 +65,37 @@ def test_oracle_rejects_bad_arguments():
 # ---- mutation check: each planted mistake must fail an independent pin -------------------------
 
 MUTANTS = {
-    "score_sign_flipped": ("s[j] = J->scale * dot;", "s[j] = -J->scale * dot;"),
-    "causal_off_by_one": ("if (J->causal && i + 1 < n_keys) n_keys = i + 1;",
-                          "if (J->causal && i + 2 < n_keys) n_keys = i + 2;"),
-    "max_shift_dropped": ("exp(s[j] - m)", "exp(s[j])"),
-    "scale_ignored": ("s[j] = J->scale * dot;", "s[j] = dot;"),
+    "score_sign_flipped": ("s[n] = J->scale * dot;", "s[n] = -J->scale * dot;"),
+    "causal_off_by_one": ("case ORC_MASK_CAUSAL: return j <= i + J->offset;",
+                          "case ORC_MASK_CAUSAL: return j <= i + J->offset + 1;"),
+    "max_shift_dropped": ("exp(s[n] - m)", "exp(s[n])"),
+    "scale_ignored": ("s[n] = J->scale * dot;", "s[n] = dot;"),
     "dot_term_dropped": ("for (int64_t d = 0; d < J->D_qk; ++d)\n            dot +=",
                          "for (int64_t d = 1; d < J->D_qk; ++d)\n            dot +="),
-    "value_rows_reversed": ("const int64_t v0 = (bh * J->S_k + j) * J->D_v;",
-                            "const int64_t v0 = (bh * J->S_k + (n_keys - 1 - j)) * J->D_v;"),
-    "key_head_ignored": ("const int64_t k0 = (bh * J->S_k + j) * J->D_qk;",
-                         "const int64_t k0 = ((b * J->H) * J->S_k + j) * J->D_qk;"),
-    "normalisation_dropped": ("const double w = exp(s[j] - m) / l;", "const double w = exp(s[j] - m);"),
-    "query_row_fixed": ("const int64_t q0 = (bh * J->S_q + i) * J->D_qk;",
-                        "const int64_t q0 = (bh * J->S_q + 0) * J->D_qk;"),
+    "value_rows_reversed": ("const int64_t v0 = (kv * J->S_k + keys[n]) * J->D_v;",
+                            "const int64_t v0 = (kv * J->S_k + keys[n_keys - 1 - n]) * J->D_v;"),
+    "key_head_ignored": ("const int64_t k0 = (kv * J->S_k + j) * J->D_qk;",
+                         "const int64_t k0 = ((b * J->H_kv) * J->S_k + j) * J->D_qk;"),
+    "normalisation_dropped": ("const double w = exp(s[n] - m) / l;", "const double w = exp(s[n] - m);"),
+    "query_row_fixed": ("const int64_t q0 = ((b * J->H + h) * J->S_q + i) * J->D_qk;",
+                        "const int64_t q0 = ((b * J->H + h) * J->S_q + 0) * J->D_qk;"),
     "bf16_widening_shift": ("<< 16", "<< 15"),
-    "noop_control": ("if (J->causal && i + 1 < n_keys) n_keys = i + 1;\n",
-                     "if (J->causal && i + 1 < n_keys) n_keys = i + 1;\n    if (J->causal) n_keys = n_keys;\n"),
+    # grouped heads, offsets, windows and the log-sum-exp
+    "kv_head_modulo": ("const int64_t g = h / (J->H / J->H_kv);", "const int64_t g = h % J->H_kv;"),
+    "offset_ignored": ("case ORC_MASK_CAUSAL: return j <= i + J->offset;", "case ORC_MASK_CAUSAL: return j <= i;"),
+    "offset_sign_flipped": ("case ORC_MASK_CAUSAL: return j <= i + J->offset;",
+                            "case ORC_MASK_CAUSAL: return j + J->offset <= i;"),
+    "window_too_wide": ("return i + J->offset - J->window < j && j <= i + J->offset;",
+                        "return i + J->offset - J->window <= j && j <= i + J->offset;"),
+    "window_without_offset": ("return i + J->offset - J->window < j && j <= i + J->offset;",
+                              "return i - J->window < j && j <= i;"),
+    "complement_off_by_one": ("case ORC_MASK_WINDOW_COMPLEMENT: return j <= i + J->offset - J->window;",
+                              "case ORC_MASK_WINDOW_COMPLEMENT: return j < i + J->offset - J->window;"),
+    "lse_max_dropped": ("*lse = n_keys > 0 ? m + log(l) : -INFINITY;", "*lse = n_keys > 0 ? log(l) : -INFINITY;"),
+    "lse_base2": ("*lse = n_keys > 0 ? m + log(l) : -INFINITY;", "*lse = n_keys > 0 ? m + log2(l) : -INFINITY;"),
+    "empty_row_lse_zero": ("*lse = n_keys > 0 ? m + log(l) : -INFINITY;", "*lse = n_keys > 0 ? m + log(l) : 0.0;"),
+    "noop_control": ("case ORC_MASK_CAUSAL: return j <= i + J->offset;\n",
+                     "case ORC_MASK_CAUSAL: return j <= i + J->offset + 0;\n"),
 }
 # "noop_control" changes nothing; it is checked to pass every pin (the harness itself is sound).
 CONTROL = "noop_control"
