@@ -2,7 +2,10 @@
 """Benchmark of the attention forward on GB300: one JSON line on stdout (rank 0).
 
 A step is one vt_attn_fwd call over the whole workload (default: B=8, H=16,
-S_q=S_k=8192, D=128, bf16, causal, Q ~ N(0, 4^2), K, V ~ N(0, 1), seed 4).
+S_q=S_k=8192, D=128, bf16, causal, Q ~ N(0, 4^2), K, V ~ N(0, 1), seed 4).  The masked and
+grouped-head workloads (--workload bf16_gqa_causal_8k, bf16_prefill_on_cache_8k,
+bf16_window_1k_8k) call vt_attn_fwd_general instead and count 2*(D_qk+D_v) flops per
+(query, key) pair their mask keeps.
 
   value        TFLOP/s over the timed steps, inputs resident in HBM (flops = 4*B*H*S_q*S_k*D,
                halved for causal; 2*B*H*S_q*S_k*(D_qk+D_v) in general), CUDA events on the
@@ -158,6 +161,20 @@ def barrier(world: int):
         dist.barrier()
 
 
+def workload_flops(w, causal: bool) -> float:
+    """Flops of one step: the metric's convention for plain workloads, kept pairs for masked ones."""
+    return w.flops_masked() if w.mask else w.flops(causal)
+
+
+def mode_of(w, causal: bool) -> str:
+    if not w.mask:
+        return f"causal={causal}"
+    extra = f", offset {w.offset}" if w.offset else ""
+    extra += f", window {w.window}" if w.mask.startswith("window") else ""
+    heads = f", H_kv {w.kv_heads}" if w.kv_heads != w.H else ""
+    return f"mask {w.mask}{extra}{heads}"
+
+
 def cpu_oracle_sample(w, q, k, v, causal: bool, target_s: float = 12.0, max_slices: int = 32):
     """Time the fp64 oracle on whole (b, h) slices of the workload until ~target_s seconds have passed."""
     import oracle
@@ -169,14 +186,17 @@ def cpu_oracle_sample(w, q, k, v, causal: bool, target_s: float = 12.0, max_slic
         b %= w.B
         rows = np.stack([np.full(rows_per_slice, b), np.full(rows_per_slice, h), np.arange(rows_per_slice)], axis=1)
         t0 = time.perf_counter()
-        oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
+        if w.mask:
+            oracle.attn_general(q, k, v, w.scale, w.mask, w.offset, w.window, rows=rows, nthreads=nthreads)
+        else:
+            oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
         t_total += time.perf_counter() - t0
-        done_flops += w.flops(causal) / (w.B * w.H)
+        done_flops += workload_flops(w, causal) / (w.B * w.H)
         slices += 1
         if t_total >= target_s:
             break
     return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{slices} whole (b,h) slice(s) of {w.name} ({w.S_q} rows each, causal={causal}), "
+            "sample": f"{slices} whole (b,h) slice(s) of {w.name} ({w.S_q} rows each, {mode_of(w, causal)}), "
                       f"{t_total:.1f} s fp64 on {nthreads} host threads"}
 
 
@@ -187,34 +207,37 @@ def run_reference(args, w, causal):
     q, k, v = synth.make_workload(w)
     import oracle
     nthreads = oracle.default_threads()
-    slice_flops = w.flops(causal) / (w.B * w.H)
     rows_per_step = max(1, min(w.S_q, int(args.ref_rows)))
     # each step: the oracle over `rows_per_step` rows spread over one (b, h) slice
     step_rows = np.linspace(0, w.S_q - 1, rows_per_step).astype(np.int64)
-    if causal:
+    if w.mask:
+        step_flops = float(w.keys_per_row()[step_rows].sum()) * 2.0 * (w.D_qk + w.D_v)
+    elif causal:
         step_flops = float(sum(2.0 * (i + 1) * (w.D_qk + w.D_v) for i in step_rows))
     else:
         step_flops = 2.0 * rows_per_step * w.S_k * (w.D_qk + w.D_v)
-    del slice_flops
     times = []
     for it in range(args.warmup + args.steps):
         b, h = divmod(it % (w.B * w.H), w.H)
         rows = np.stack([np.full(len(step_rows), b), np.full(len(step_rows), h), step_rows], axis=1)
         t0 = time.perf_counter()
-        oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
+        if w.mask:
+            oracle.attn_general(q, k, v, w.scale, w.mask, w.offset, w.window, rows=rows, nthreads=nthreads)
+        else:
+            oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
         dt = time.perf_counter() - t0
         if it >= args.warmup:
             times.append(dt)
     total = sum(times)
     value = step_flops * len(times) / total / 1e12
     sample = (f"{rows_per_step} query rows evenly spread over one (b,h) slice of {w.name} per step "
-              f"(causal={causal}), fp64 on {nthreads} host threads")
+              f"({mode_of(w, causal)}), fp64 on {nthreads} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "S_q": w.S_q, "S_k": w.S_k, "D_qk": w.D_qk,
-                   "D_v": w.D_v, "causal": causal, "io_dtype": w.dtype},
+                   "D_v": w.D_v, "causal": causal, "io_dtype": w.dtype, "mode": mode_of(w, causal)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -270,11 +293,22 @@ def main() -> int:
     hO = torch.empty(O.shape, dtype=tdt).pin_memory()
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    flops = w.flops(causal)
+    flops = workload_flops(w, causal)
+    mask = vt.vt_attn_mask(vt.MASKS[w.mask], 0, w.offset, w.window) if w.mask else None
+
+    def call(q_, k_, v_, o_, stream_handle):
+        """One forward through the C ABI: vt_attn_fwd, or the general entry point for masked or
+        grouped-head workloads."""
+        if mask is None:
+            return vt.vt_attn_fwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), w.B, w.H, w.S_q,
+                                  w.S_k, w.D_qk, w.D_v, w.scale, int(causal), vt_dtype, stream_handle)
+        return vt.vt_attn_fwd_general(q_.data_ptr(), q_.stride()[:3], k_.data_ptr(), k_.stride()[:3],
+                                      v_.data_ptr(), v_.stride()[:3], o_.data_ptr(), o_.stride()[:3], None, w.B,
+                                      w.H, w.kv_heads, w.S_q, w.S_k, w.D_qk, w.D_v, w.scale, vt_dtype, mask, 1,
+                                      None, 0, None, stream_handle)
 
     def step():
-        rc = vt.vt_attn_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), w.B, w.H, w.S_q, w.S_k,
-                            w.D_qk, w.D_v, w.scale, int(causal), vt_dtype, sh)
+        rc = call(Q, K, V, O, sh)
         if rc != 0:
             raise RuntimeError(f"vt_attn_fwd: {vt.vt_status_str(rc)}")
 
@@ -333,8 +367,7 @@ def main() -> int:
         s_cmp.wait_event(ev_in[b])
         if i >= 2:
             s_cmp.wait_event(ev_out[b])  # O_b is free once step i-2's result has been read back
-        rc = vt.vt_attn_fwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), w.B, w.H, w.S_q, w.S_k,
-                            w.D_qk, w.D_v, w.scale, int(causal), vt_dtype, s_cmp.cuda_stream)
+        rc = call(q_, k_, v_, o_, s_cmp.cuda_stream)
         if rc != 0:
             raise RuntimeError(f"vt_attn_fwd: {vt.vt_status_str(rc)}")
         ev_cmp[b].record(s_cmp)
@@ -379,7 +412,8 @@ def main() -> int:
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "S_q": w.S_q, "S_k": w.S_k, "D_qk": w.D_qk,
-                       "D_v": w.D_v, "causal": causal, "flops_per_step": flops,
+                       "D_v": w.D_v, "causal": causal, "mode": mode_of(w, causal), "H_kv": w.kv_heads,
+                       "flops_per_step": flops,
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "peak_frac": value / world / peak,

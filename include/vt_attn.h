@@ -186,6 +186,64 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3],
                                       float scale, int causal, vt_dtype dtype,
                                       int n_split, vt_stream_t stream);
 
+/*
+ * General form.  Everything above is a special case of vt_attn_fwd_general, which adds:
+ *
+ * Grouped key/value heads (GQA; H_kv = 1 is multi-query attention).  K is [B,H_kv,S_k,D_qk] and V
+ * is [B,H_kv,S_k,D_v]; query head h < H reads key/value head h / (H / H_kv), the num_kv_heads
+ * indexing of the VeriTile coverage table's block-sparse attention row.  H must be a multiple of
+ * H_kv; k_stride and v_stride are the strides of (b, h_kv, s).
+ *
+ * A mask choosing the keys A_i of query row i (o = offset >= 0, w = window >= 1):
+ *   VT_MASK_NONE               A_i = { j < S_k }
+ *   VT_MASK_CAUSAL             A_i = { j < S_k : j <= i + o }; query i sits at key position i + o
+ *                              (the start_position of the coverage table's attention_llama causal
+ *                              row; o = S_k - S_q aligns the last query with the last key)
+ *   VT_MASK_WINDOW             A_i = { j < S_k : i + o - w < j <= i + o }: the w most recent keys
+ *                              (the sliding window of the coverage table's attention_fwd_triton3
+ *                              row, case 1)
+ *   VT_MASK_WINDOW_COMPLEMENT  A_i = { j < S_k : j <= i + o - w }: the causal keys the window leaves
+ *                              out (case 2 of the same row)
+ * Key tiles outside every row's A_i are skipped, not masked.  A row whose A_i is empty (possible
+ * with the window kinds only) is written as 0.
+ *
+ * An optional log-sum-exp output: lse, if not NULL, is a DEVICE fp32 array [B,H,S_q] (packed,
+ * row-major) that receives LSE[b,h,i] = log(sum_{j in A_i} exp(scale * Q_i . K_j)), natural log,
+ * -inf for an empty row.  With it, two calls over disjoint key sets (a window and its complement,
+ * or two key ranges) combine into the call over their union: O = sum_k e^{LSE_k} O_k / sum_k e^{LSE_k}
+ * (the continuation case 4 of the attention_fwd_triton3 row).  Must be 4-byte aligned and must not
+ * overlap Q, K, V, O or the workspace.
+ *
+ * n_split, workspace and workspace_bytes are those of vt_attn_fwd_splitkv (n_split > 1: bf16 only);
+ * opts those of vt_attn_fwd_ex (may be NULL); mask may be NULL (VT_MASK_NONE).  Errors as for
+ * vt_attn_fwd_splitkv, and VT_ERR_INVALID_ARG for H_kv < 1, H not a multiple of H_kv, an unknown mask
+ * kind, offset < 0, window < 1 with a window kind, or a misplaced lse; VT_ERR_UNSUPPORTED for
+ * offset or window above 2^40.
+ */
+typedef enum {
+    VT_MASK_NONE = 0,
+    VT_MASK_CAUSAL = 1,
+    VT_MASK_WINDOW = 2,
+    VT_MASK_WINDOW_COMPLEMENT = 3
+} vt_mask_kind;
+
+typedef struct {
+    int32_t kind;     /* vt_mask_kind */
+    int32_t reserved; /* 0 */
+    int64_t offset;   /* o >= 0 */
+    int64_t window;   /* w >= 1 for the window kinds; ignored otherwise */
+} vt_attn_mask;
+
+vt_status vt_attn_fwd_general(const void *Q, const int64_t q_stride[3],
+                              const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3],
+                              void *O, const int64_t o_stride[3], float *lse,
+                              int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_k,
+                              int64_t D_qk, int64_t D_v, float scale, vt_dtype dtype,
+                              const vt_attn_mask *mask, int n_split,
+                              void *workspace, size_t workspace_bytes,
+                              const vt_attn_opts *opts, vt_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *vt_status_str(vt_status status);
 

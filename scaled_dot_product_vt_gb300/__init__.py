@@ -15,6 +15,9 @@ from ._build import LIB, build  # noqa: F401
 
 VT_F32, VT_BF16 = 0, 1
 VT_OPT_TEST_STALL = 1
+VT_MASK_NONE, VT_MASK_CAUSAL, VT_MASK_WINDOW, VT_MASK_WINDOW_COMPLEMENT = 0, 1, 2, 3
+MASKS = {"none": VT_MASK_NONE, "causal": VT_MASK_CAUSAL, "window": VT_MASK_WINDOW,
+         "window_complement": VT_MASK_WINDOW_COMPLEMENT}
 
 STATUS = {
     0: "VT_OK", 1: "VT_ERR_INVALID_ARG", 2: "VT_ERR_UNSUPPORTED", 3: "VT_ERR_MISALIGNED",
@@ -24,7 +27,7 @@ STATUS = {
 # Every symbol the header declares.
 EXPORTS = ("vt_attn_fwd", "vt_attn_fwd_strided", "vt_attn_fwd_ex", "vt_attn_fwd_splitkv",
            "vt_attn_splitkv_workspace_size", "vt_attn_splitkv_choose", "vt_attn_fwd_splitkv_noalloc",
-           "vt_status_str", "vt_last_device_status")
+           "vt_attn_fwd_general", "vt_status_str", "vt_last_device_status")
 
 
 class VtError(RuntimeError):
@@ -35,6 +38,11 @@ class VtError(RuntimeError):
 
 class vt_attn_opts(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_uint64), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class vt_attn_mask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("reserved", ctypes.c_int32), ("offset", ctypes.c_int64),
+                ("window", ctypes.c_int64)]
 
 
 _lib = None
@@ -69,6 +77,9 @@ def load(path: str | None = None):
     lib.vt_attn_fwd_splitkv_noalloc.argtypes = [vp, st3, vp, st3, vp, st3, vp, st3, i64, i64, i64, i64, i64, i64,
                                                 f, i, i, i, vp]
     lib.vt_attn_fwd_splitkv_noalloc.restype = i
+    lib.vt_attn_fwd_general.argtypes = [vp, st3, vp, st3, vp, st3, vp, st3, vp, i64, i64, i64, i64, i64, i64, i64, f,
+                                        i, ctypes.POINTER(vt_attn_mask), i, vp, sz, ctypes.POINTER(vt_attn_opts), vp]
+    lib.vt_attn_fwd_general.restype = i
     lib.vt_status_str.argtypes = [i]
     lib.vt_status_str.restype = ctypes.c_char_p
     lib.vt_last_device_status.argtypes = [vp]
@@ -125,6 +136,16 @@ def vt_attn_fwd_splitkv_noalloc(Q, q_stride, K, k_stride, V, v_stride, O, o_stri
     return load().vt_attn_fwd_splitkv_noalloc(Q, _stride3(q_stride), K, _stride3(k_stride), V, _stride3(v_stride),
                                               O, _stride3(o_stride), B, H, S_q, S_k, D_qk, D_v, scale, int(causal),
                                               dtype, int(n_split), stream)
+
+
+def vt_attn_fwd_general(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, lse, B, H, H_kv, S_q, S_k, D_qk, D_v,
+                        scale, dtype, mask, n_split, workspace, workspace_bytes, opts, stream) -> int:
+    """The general C entry point with raw device addresses (ints; lse and workspace may be None);
+    ``mask`` is a vt_attn_mask or None.  Returns the vt_status code."""
+    return load().vt_attn_fwd_general(Q, _stride3(q_stride), K, _stride3(k_stride), V, _stride3(v_stride), O,
+                                      _stride3(o_stride), lse, B, H, H_kv, S_q, S_k, D_qk, D_v, scale, dtype,
+                                      ctypes.byref(mask) if mask is not None else None, int(n_split), workspace,
+                                      int(workspace_bytes), ctypes.byref(opts) if opts is not None else None, stream)
 
 
 def vt_status_str(code: int) -> str:
@@ -215,3 +236,41 @@ def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, 
     if rc != 0:
         raise VtError(rc, "vt_attn_fwd_splitkv")
     return out
+
+
+def attn_fwd_general(q, k, v, scale: float | None = None, mask: str = "none", offset: int = 0, window: int = 0,
+                     return_lse: bool = False, n_split: int = 1, out=None, lse=None, workspace=None, stream=None,
+                     opts=None):
+    """General forward for CUDA tensors: q [B,H,S_q,D_qk], k [B,H_kv,S_k,D_qk], v [B,H_kv,S_k,D_v] with H a
+    multiple of H_kv (grouped heads), ``mask`` one of ``MASKS`` with ``offset`` and ``window`` (see
+    include/vt_attn.h).  Returns O, or (O, LSE) with ``return_lse`` (LSE: float32 [B,H,S_q], natural log).
+    ``n_split`` > 1 runs the split-KV form (bf16); its workspace is allocated here unless given."""
+    import torch
+    B, H, S_q, D_qk = q.shape
+    H_kv, S_k, D_v = k.shape[1], k.shape[2], v.shape[3]
+    if k.shape != (B, H_kv, S_k, D_qk) or v.shape != (B, H_kv, S_k, D_v):
+        raise ValueError("shape mismatch between q, k and v")
+    code = _dtype_code(q)
+    if _dtype_code(k) != code or _dtype_code(v) != code:
+        raise TypeError("q, k and v must share one dtype")
+    if scale is None:
+        scale = float(D_qk) ** -0.5
+    if out is None:
+        out = torch.empty((B, H, S_q, D_v), dtype=q.dtype, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * S_q):
+        raise ValueError("lse must be a contiguous float32 tensor of B*H*S_q elements")
+    need = vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    m = vt_attn_mask(MASKS[mask], 0, int(offset), int(window))
+    rc = vt_attn_fwd_general(q.data_ptr(), _bhs_strides(q), k.data_ptr(), _bhs_strides(k), v.data_ptr(),
+                             _bhs_strides(v), out.data_ptr(), _bhs_strides(out),
+                             lse.data_ptr() if lse is not None else None, B, H, H_kv, S_q, S_k, D_qk, D_v,
+                             float(scale), code, m, n_split, ws_ptr, ws_bytes, opts, _stream_handle(stream))
+    if rc != 0:
+        raise VtError(rc, "vt_attn_fwd_general")
+    return (out, lse) if return_lse else out

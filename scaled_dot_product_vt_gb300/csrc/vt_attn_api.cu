@@ -149,19 +149,46 @@ SplitLayout split_layout(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_s
     return L;
 }
 
+// One forward problem as the general entry point states it (include/vt_attn.h).
+struct Problem {
+    const void *Q, *K, *V;
+    void *O;
+    const int64_t *qs, *ks, *vs, *os;  // (b, h, s) element strides; K and V count key/value heads
+    float *lse;                        // nullptr or [B*H*S_q]
+    int64_t B, H, H_kv, S_q, S_k, D_qk, D_v;
+    float scale;
+    vt_dtype dtype;
+    int mask;
+    int64_t offset, window;
+};
+
+constexpr int64_t kMaxBandArg = int64_t(1) << 40;
+
+// The band [i + lo, i + hi] of each mask kind, and whether later query blocks carry more work.
+void band_of(const Problem &P, long long *lo, long long *hi, int *reverse) {
+    switch (P.mask) {
+        case VT_MASK_CAUSAL: *lo = -kBandInf; *hi = P.offset; *reverse = 1; return;
+        case VT_MASK_WINDOW: *lo = P.offset - P.window + 1; *hi = P.offset; *reverse = 0; return;
+        case VT_MASK_WINDOW_COMPLEMENT: *lo = -kBandInf; *hi = P.offset - P.window; *reverse = 1; return;
+        default: *lo = -kBandInf; *hi = kBandInf; *reverse = 0; return;
+    }
+}
+
 template <int DT>
-vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
-                 const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
-                 int64_t D_qk, int64_t D_v, float scale, int causal, const vt_attn_opts *opts, int n_split,
-                 void *workspace, cudaStream_t stream) {
+vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *workspace, cudaStream_t stream) {
     using C = Cfg<DT>;
+    const void *Q = P.Q, *K = P.K, *V = P.V;
+    void *O = P.O;
+    const int64_t *qs = P.qs, *ks = P.ks, *vs = P.vs, *os = P.os;
+    const int64_t B = P.B, H = P.H, S_q = P.S_q, S_k = P.S_k, D_qk = P.D_qk, D_v = P.D_v;
     CUtensorMap tq, tk, tv;
     // K/V boxes are one key tile high
     const int kv_rows = DT == kBF16 ? q2::kBN : C::kBN;
-    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) || !make_map(&tk, K, ks, B, H, S_k, D_qk, C::kElt, kv_rows))
+    if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) ||
+        !make_map(&tk, K, ks, B, P.H_kv, S_k, D_qk, C::kElt, kv_rows))
         return VT_ERR_CUDA;
     if (DT == kBF16) {
-        if (!make_map(&tv, V, vs, B, H, S_k, D_v, C::kElt, kv_rows)) return VT_ERR_CUDA;
+        if (!make_map(&tv, V, vs, B, P.H_kv, S_k, D_v, C::kElt, kv_rows)) return VT_ERR_CUDA;
     } else {
         tv = tk;  // fp32: V is read by the kernel's transposing loader warps, not by TMA
     }
@@ -178,8 +205,10 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
     p.q_chunks = static_cast<int>((D_qk + C::kChunkElems - 1) / C::kChunkElems);
     p.v_chunks = static_cast<int>((D_v + C::kChunkElems - 1) / C::kChunkElems);
     p.n_pv = static_cast<int>((D_v + 15) / 16 * 16);
-    p.causal = causal ? 1 : 0;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    band_of(P, &p.band_lo, &p.band_hi, &p.reverse_q);
+    p.kv_group = static_cast<int>(H / P.H_kv);
+    p.lse = P.lse;
+    p.scale_log2 = P.scale * 1.4426950408889634f;
     p.O = O;
     p.o_sb = os[0];
     p.o_sh = os[1];
@@ -237,6 +266,7 @@ vt_status launch(const void *Q, const int64_t qs[3], const void *K, const int64_
             mp.part_m = p.part_m;
             mp.part_l = p.part_l;
             mp.O = O;
+            mp.lse = P.lse;
             mp.rows = B * H * S_q;
             mp.H = static_cast<int>(H);
             mp.S_q = static_cast<int>(S_q);
@@ -332,15 +362,18 @@ namespace {
 
 // Argument checks shared by every forward entry point (see include/vt_attn.h); VT_OK with
 // *empty = true for a valid empty problem.
-vt_status check_args(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
-                     const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
-                     int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, vt_dtype dtype,
-                     bool *empty) {
+vt_status check_args(const Problem &P, bool *empty) {
     *empty = false;
-    if (dtype != VT_F32 && dtype != VT_BF16) return VT_ERR_INVALID_ARG;
+    const int64_t B = P.B, H = P.H, H_kv = P.H_kv, S_q = P.S_q, S_k = P.S_k, D_qk = P.D_qk, D_v = P.D_v;
+    if (P.dtype != VT_F32 && P.dtype != VT_BF16) return VT_ERR_INVALID_ARG;
     if (B < 0 || H < 0 || S_q < 0 || S_k < 0 || D_qk < 0 || D_v < 0) return VT_ERR_INVALID_ARG;
     if (S_k == 0 || D_qk == 0 || D_v == 0) return VT_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return VT_ERR_INVALID_ARG;
+    if (H_kv < 1 || (H > 0 && H % H_kv != 0)) return VT_ERR_INVALID_ARG;
+    if (!std::isfinite(P.scale)) return VT_ERR_INVALID_ARG;
+    if (P.mask < VT_MASK_NONE || P.mask > VT_MASK_WINDOW_COMPLEMENT || P.offset < 0) return VT_ERR_INVALID_ARG;
+    const bool windowed = P.mask == VT_MASK_WINDOW || P.mask == VT_MASK_WINDOW_COMPLEMENT;
+    if (windowed && P.window < 1) return VT_ERR_INVALID_ARG;
+    if (P.offset > vt::kMaxBandArg || (windowed && P.window > vt::kMaxBandArg)) return VT_ERR_UNSUPPORTED;
     if (D_qk > vt::kMaxD || D_v > vt::kMaxD) return VT_ERR_UNSUPPORTED;
     if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxExtent || S_k > vt::kMaxExtent)
         return VT_ERR_UNSUPPORTED;
@@ -348,37 +381,77 @@ vt_status check_args(const void *Q, const int64_t q_stride[3], const void *K, co
         *empty = true;
         return VT_OK;
     }
-    if (!Q || !K || !V || !O || !q_stride || !k_stride || !v_stride || !o_stride) return VT_ERR_INVALID_ARG;
-    const int elt = dtype == VT_BF16 ? 2 : 4;
-    const int64_t *st[4] = {q_stride, k_stride, v_stride, o_stride};
+    if (!P.Q || !P.K || !P.V || !P.O || !P.qs || !P.ks || !P.vs || !P.os) return VT_ERR_INVALID_ARG;
+    const int elt = P.dtype == VT_BF16 ? 2 : 4;
+    const int64_t *st[4] = {P.qs, P.ks, P.vs, P.os};
     for (const int64_t *s : st)
         for (int i = 0; i < 3; ++i)
             if (s[i] <= 0) return VT_ERR_INVALID_ARG;
-    const void *ptrs[4] = {Q, K, V, O};
+    const void *ptrs[4] = {P.Q, P.K, P.V, P.O};
     for (const void *ptr : ptrs)
         if (reinterpret_cast<uintptr_t>(ptr) % 16) return VT_ERR_MISALIGNED;
     for (const int64_t *s : st)
         for (int i = 0; i < 3; ++i)
             if ((s[i] * elt) % 16) return VT_ERR_MISALIGNED;
-    const vt::Span so = vt::span_of(O, o_stride, B, H, S_q, D_v, elt);
-    if (vt::overlap(so, vt::span_of(Q, q_stride, B, H, S_q, D_qk, elt)) ||
-        vt::overlap(so, vt::span_of(K, k_stride, B, H, S_k, D_qk, elt)) ||
-        vt::overlap(so, vt::span_of(V, v_stride, B, H, S_k, D_v, elt)))
-        return VT_ERR_INVALID_ARG;
+    const vt::Span sq = vt::span_of(P.Q, P.qs, B, H, S_q, D_qk, elt);
+    const vt::Span sk = vt::span_of(P.K, P.ks, B, H_kv, S_k, D_qk, elt);
+    const vt::Span sv = vt::span_of(P.V, P.vs, B, H_kv, S_k, D_v, elt);
+    const vt::Span so = vt::span_of(P.O, P.os, B, H, S_q, D_v, elt);
+    if (vt::overlap(so, sq) || vt::overlap(so, sk) || vt::overlap(so, sv)) return VT_ERR_INVALID_ARG;
+    if (P.lse) {
+        if (reinterpret_cast<uintptr_t>(P.lse) % 4) return VT_ERR_INVALID_ARG;
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(P.lse);
+        const vt::Span sl{lo, lo + static_cast<uintptr_t>(B * H * S_q) * sizeof(float)};
+        if (vt::overlap(sl, sq) || vt::overlap(sl, sk) || vt::overlap(sl, sv) || vt::overlap(sl, so))
+            return VT_ERR_INVALID_ARG;
+    }
     return VT_OK;
 }
 
-vt_status forward(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
-                  const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
-                  int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype, const vt_attn_opts *opts,
-                  int n_split, void *workspace, cudaStream_t s) {
-    const vt_status r = dtype == VT_BF16
-                            ? launch<kBF16>(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, opts,
-                                            n_split, workspace, s)
-                            : launch<kF32>(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, opts,
-                                           n_split, workspace, s);
+// Checks of a split-KV workspace (n_split > 1): present, large enough, 256-byte aligned and clear of
+// every tensor of the call.
+vt_status check_workspace(const Problem &P, int n_split, const void *workspace, size_t workspace_bytes) {
+    if (P.dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < vt::split_layout(P.B, P.H, P.S_q, P.D_v, n_split).bytes)
+        return VT_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return VT_ERR_MISALIGNED;
+    const vt::Span w{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + workspace_bytes};
+    const int elt = 2;
+    if (vt::overlap(w, vt::span_of(P.Q, P.qs, P.B, P.H, P.S_q, P.D_qk, elt)) ||
+        vt::overlap(w, vt::span_of(P.K, P.ks, P.B, P.H_kv, P.S_k, P.D_qk, elt)) ||
+        vt::overlap(w, vt::span_of(P.V, P.vs, P.B, P.H_kv, P.S_k, P.D_v, elt)) ||
+        vt::overlap(w, vt::span_of(P.O, P.os, P.B, P.H, P.S_q, P.D_v, elt)))
+        return VT_ERR_INVALID_ARG;
+    if (P.lse) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(P.lse);
+        if (vt::overlap(w, vt::Span{lo, lo + static_cast<uintptr_t>(P.B * P.H * P.S_q) * sizeof(float)}))
+            return VT_ERR_INVALID_ARG;
+    }
+    return VT_OK;
+}
+
+vt_status forward(const Problem &P, const vt_attn_opts *opts, int n_split, void *workspace, cudaStream_t s) {
+    const vt_status r = P.dtype == VT_BF16 ? launch<kBF16>(P, opts, n_split, workspace, s)
+                                           : launch<kF32>(P, opts, n_split, workspace, s);
     if (r != VT_OK) return r;
     return env_check() ? read_status(s) : VT_OK;
+}
+
+// The problem of the entry points that predate the general form: H_kv = H, no lse, causal or not.
+Problem plain_problem(const void *Q, const int64_t qs[3], const void *K, const int64_t ks[3], const void *V,
+                      const int64_t vs[3], void *O, const int64_t os[3], int64_t B, int64_t H, int64_t S_q,
+                      int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype) {
+    Problem P{};
+    P.Q = Q; P.K = K; P.V = V; P.O = O;
+    P.qs = qs; P.ks = ks; P.vs = vs; P.os = os;
+    P.lse = nullptr;
+    P.B = B; P.H = H; P.H_kv = H > 0 ? H : 1; P.S_q = S_q; P.S_k = S_k; P.D_qk = D_qk; P.D_v = D_v;
+    P.scale = scale;
+    P.dtype = dtype;
+    P.mask = causal ? VT_MASK_CAUSAL : VT_MASK_NONE;
+    P.offset = 0;
+    P.window = 0;
+    return P;
 }
 
 }  // namespace
@@ -390,12 +463,41 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K
                          const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
                          int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
                          vt_dtype dtype, const vt_attn_opts *opts, vt_stream_t stream) {
+    const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
+                                            D_v, scale, causal, dtype);
     bool empty = false;
-    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
-                                       scale, dtype, &empty);
+    const vt_status c = vt::check_args(P, &empty);
     if (c != VT_OK || empty) return c;
-    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
-                       dtype, opts, 1, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return vt::forward(P, opts, 1, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+vt_status vt_attn_fwd_general(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],
+                              const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3],
+                              float *lse, int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_k, int64_t D_qk,
+                              int64_t D_v, float scale, vt_dtype dtype, const vt_attn_mask *mask, int n_split,
+                              void *workspace, size_t workspace_bytes, const vt_attn_opts *opts,
+                              vt_stream_t stream) {
+    vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
+                                      scale, 0, dtype);
+    P.H_kv = H_kv;
+    P.lse = lse;
+    if (mask) {
+        if (mask->reserved != 0) return VT_ERR_INVALID_ARG;
+        P.mask = mask->kind;
+        P.offset = mask->offset;
+        P.window = mask->window;
+    }
+    bool empty = false;
+    const vt_status c = vt::check_args(P, &empty);
+    if (c != VT_OK) return c;
+    if (n_split < 1) return VT_ERR_INVALID_ARG;
+    if (n_split > vt::kMaxSplit) return VT_ERR_UNSUPPORTED;
+    if (empty) return VT_OK;
+    if (n_split > 1) {
+        const vt_status w = vt::check_workspace(P, n_split, workspace, workspace_bytes);
+        if (w != VT_OK) return w;
+    }
+    return vt::forward(P, opts, n_split, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split) {
@@ -424,29 +526,19 @@ vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3], const vo
                               int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
                               vt_dtype dtype, int n_split, void *workspace, size_t workspace_bytes,
                               vt_stream_t stream) {
+    const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
+                                            D_v, scale, causal, dtype);
     bool empty = false;
-    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
-                                       scale, dtype, &empty);
+    const vt_status c = vt::check_args(P, &empty);
     if (c != VT_OK) return c;
     if (n_split < 1) return VT_ERR_INVALID_ARG;
     if (n_split > vt::kMaxSplit) return VT_ERR_UNSUPPORTED;
     if (empty) return VT_OK;
     if (n_split > 1) {
-        if (dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
-        if (!workspace || workspace_bytes < vt::split_layout(B, H, S_q, D_v, n_split).bytes)
-            return VT_ERR_INVALID_ARG;
-        if (reinterpret_cast<uintptr_t>(workspace) % 256) return VT_ERR_MISALIGNED;
-        // the partial outputs must not overlap any tensor of the call
-        const vt::Span w{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + workspace_bytes};
-        const int elt = 2;
-        if (vt::overlap(w, vt::span_of(Q, q_stride, B, H, S_q, D_qk, elt)) ||
-            vt::overlap(w, vt::span_of(K, k_stride, B, H, S_k, D_qk, elt)) ||
-            vt::overlap(w, vt::span_of(V, v_stride, B, H, S_k, D_v, elt)) ||
-            vt::overlap(w, vt::span_of(O, o_stride, B, H, S_q, D_v, elt)))
-            return VT_ERR_INVALID_ARG;
+        const vt_status w = vt::check_workspace(P, n_split, workspace, workspace_bytes);
+        if (w != VT_OK) return w;
     }
-    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
-                       dtype, nullptr, n_split, workspace, reinterpret_cast<cudaStream_t>(stream));
+    return vt::forward(P, nullptr, n_split, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], const void *K,
@@ -454,9 +546,10 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], 
                                       const int64_t o_stride[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
                                       int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype, int n_split,
                                       vt_stream_t stream) {
+    const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
+                                            D_v, scale, causal, dtype);
     bool empty = false;
-    const vt_status c = vt::check_args(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
-                                       scale, dtype, &empty);
+    const vt_status c = vt::check_args(P, &empty);
     if (c != VT_OK) return c;
     if (n_split < 1) return VT_ERR_INVALID_ARG;
     if (n_split > vt::kMaxSplit) return VT_ERR_UNSUPPORTED;
@@ -471,8 +564,7 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], 
         scratch = vt::noalloc_scratch(dev);
         if (!scratch) return VT_ERR_CUDA;
     }
-    return vt::forward(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale, causal,
-                       dtype, nullptr, n_split, scratch, reinterpret_cast<cudaStream_t>(stream));
+    return vt::forward(P, nullptr, n_split, scratch, reinterpret_cast<cudaStream_t>(stream));
 }
 
 vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const void *K, const int64_t k_stride[3],

@@ -96,32 +96,51 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
     const int g_heads = min(p.head_group, BH - g * p.head_group);
     const int slot_q = rr / g_heads;
     const int bh = g * p.head_group + (rr - slot_q * g_heads);
-    const int qb = p.causal ? (p.n_qblocks - 1 - slot_q) : slot_q;
+    const int qb = p.reverse_q ? (p.n_qblocks - 1 - slot_q) : slot_q;
     const int h = bh % p.H;
     const int b = bh / p.H;
+    const int hk = h / p.kv_group;  // key/value head
     const int r0 = qb * kRows;
 
-    // key tiles each query tile needs (0 when the tile lies past S_q)
-    const int n_all = (p.S_k + BN - 1) / BN;
-    int n0, n1, j0;
+    // Key tiles of this CTA: the union of both query tiles' ranges (contiguous: tile 1's first key
+    // never lies past tile 0's last), cut into n_split contiguous shares.  [as_t, es_t) is the part
+    // query tile t needs, relative to the share's first tile j0 (empty as 0, 0).
+    int as0, es0, as1, es1, j0, n_kv;
     {
-        int n[2];
+        int a[2], e[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const int first = r0 + t * kBM;
-            if (first >= p.S_q) n[t] = 0;
-            else if (p.causal) n[t] = min(n_all, (min(first + kBM, p.S_q) - 1) / BN + 1);
-            else n[t] = n_all;
+            if (first >= p.S_q) {
+                a[t] = 0;
+                e[t] = 0;
+            } else {
+                band_tiles(p, first, min(first + kBM, p.S_q) - 1, BN, &a[t], &e[t]);
+            }
         }
-        // this CTA's contiguous share of the item's key tiles: [j0, j_end)
-        const int n_item = max(n[0], n[1]);
+        const bool has0 = e[0] > a[0], has1 = e[1] > a[1];
+        const int A = has0 ? (has1 ? min(a[0], a[1]) : a[0]) : (has1 ? a[1] : 0);
+        const int E = has0 ? (has1 ? max(e[0], e[1]) : e[0]) : (has1 ? e[1] : 0);
+        const int n_item = E - A;
         const int per = (n_item + p.n_split - 1) / p.n_split;
         const int lo = min(split * per, n_item), hi = min(n_item, lo + per);
-        n0 = max(0, min(n[0], hi) - lo);  // key tiles of this share each query tile needs
-        n1 = max(0, min(n[1], hi) - lo);
-        j0 = lo;
+        j0 = A + lo;
+        n_kv = hi - lo;
+        int as[2], es[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            as[t] = min(max(a[t] - j0, 0), n_kv);
+            es[t] = min(max(e[t] - j0, 0), n_kv);
+            if (es[t] <= as[t]) {
+                as[t] = 0;
+                es[t] = 0;
+            }
+        }
+        as0 = as[0];
+        es0 = es[0];
+        as1 = as[1];
+        es1 = es[1];
     }
-    const int n_kv = max(n0, n1);
     const int n_slots = p.stages;
 
     // ---- shared memory: Q tile 0, Q tile 1, then `n_slots` equal K/V slots
@@ -169,11 +188,12 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_kv > 0) {
-            const int q_tiles = n1 > 0 ? 2 : 1;
-            mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_tiles * q_tile_bytes);
-            for (int c = 0; c < p.q_chunks; ++c)
-                tma_load_4d(sQ0 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0, h, b);
-            if (q_tiles == 2)
+            const bool load0 = es0 > as0, load1 = es1 > as1;  // Q tiles with work in this share
+            mbar_arrive_expect_tx(smem_u32(&ctl.q_full), (int(load0) + int(load1)) * q_tile_bytes);
+            if (load0)
+                for (int c = 0; c < p.q_chunks; ++c)
+                    tma_load_4d(sQ0 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0, h, b);
+            if (load1)
                 for (int c = 0; c < p.q_chunks; ++c)
                     tma_load_4d(sQ1 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0 + kBM, h, b);
             // loads i = 2j (K_j) and 2j + 1 (V_j) go to slot i mod n_slots
@@ -193,11 +213,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 if ((i & 1) == 0) {
                     mbar_arrive_expect_tx(bar, k_bytes);
                     for (int c = 0; c < p.q_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, (j0 + j) * BN, h, b);
+                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, (j0 + j) * BN, hk, b);
                 } else {
                     mbar_arrive_expect_tx(bar, v_bytes);
                     for (int c = 0; c < p.v_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, (j0 + j) * BN, h, b);
+                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, (j0 + j) * BN, hk, b);
                 }
                 ++loads;
                 if (++s == n_slots) s = 0;
@@ -252,15 +272,18 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 
             if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook
             if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
+            // query tile t takes part in key tile j when as_t <= j < es_t
+            auto act0 = [&](int j) { return j >= as0 && j < es0; };
+            auto act1 = [&](int j) { return j >= as1 && j < es1; };
             int ks = 0;  // slot of K_j
             if (ok) ok = wait_full(ks);
             if (ok) {
                 const uint32_t k_lo = k_lo0 + ks * slot_step;
-                if (n0 > 0) {
+                if (act0(0)) {
                     qk(s_col0, q_lo0, k_lo);
                     mma_commit(smem_u32(&ctl.s_full[0]));
                 }
-                if (n1 > 0) {
+                if (act1(0)) {
                     qk(s_col1, q_lo1, k_lo);
                     mma_commit(smem_u32(&ctl.s_full[1]));
                 }
@@ -274,28 +297,28 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 if (!(ok = wait_full(vs))) break;
                 const uint32_t v_lo = v_lo0 + vs * slot_step;
                 const uint32_t kn_lo = k_lo0 + kn * slot_step;
-                if (j < n0) {
-                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), j & 1, ctl.abort_flag, p))) break;
+                if (act0(j)) {
+                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), (j - as0) & 1, ctl.abort_flag, p))) break;
                     tc_fence_after();
-                    pv(o_col0, s_col0, v_lo, j > 0);
+                    pv(o_col0, s_col0, v_lo, j > as0);
                 }
                 if (more && !(ok = wait_full(kn))) break;
-                if (j + 1 < n0) {
+                if (act0(j + 1)) {
                     qk(s_col0, q_lo0, kn_lo);
                     mma_commit(smem_u32(&ctl.s_full[0]));
-                } else if (j < n0) {
+                } else if (act0(j)) {
                     mma_commit(smem_u32(&ctl.o_done[0]));
                 }
-                if (j < n1) {
-                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), j & 1, ctl.abort_flag, p))) break;
+                if (act1(j)) {
+                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), (j - as1) & 1, ctl.abort_flag, p))) break;
                     tc_fence_after();
-                    pv(o_col1, s_col1, v_lo, j > 0);
+                    pv(o_col1, s_col1, v_lo, j > as1);
                 }
                 mma_commit(smem_u32(&ctl.empty[vs]));
-                if (j + 1 < n1) {
+                if (act1(j + 1)) {
                     qk(s_col1, q_lo1, kn_lo);
                     mma_commit(smem_u32(&ctl.s_full[1]));
-                } else if (j < n1) {
+                } else if (act1(j)) {
                     mma_commit(smem_u32(&ctl.o_done[1]));
                 }
                 if (more) mma_commit(smem_u32(&ctl.empty[kn]));
@@ -315,7 +338,13 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         const int row = quad * 32 + lane;
         const int tile_row0 = r0 + t * kBM;
         const int q_row = tile_row0 + row;
-        const int n_my = t ? n1 : n0;
+        const int as_my = t ? as1 : as0;
+        const int n_my = (t ? es1 : es0) - as_my;
+        // this row's allowed keys [key_lo, key_hi); a key tile starting below mask_lo or ending past
+        // mask_hi cuts some row's range and is masked (the same decision for the whole warpgroup)
+        const int key_lo = band_key_lo(p, q_row), key_hi = band_key_hi(p, q_row);
+        const int mask_lo = band_key_lo(p, min(tile_row0 + kBM, p.S_q) - 1);
+        const int mask_hi = band_key_hi(p, tile_row0);
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + col_s(t);
         const uint32_t o_addr = tmem + lane_base + col_o(t);
@@ -343,12 +372,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
             }
-            const int k0 = (j0 + j) * BN;
-            if ((k0 + BN > p.S_k) || (p.causal && k0 + BN - 1 > tile_row0)) {
-                const int lim = p.causal ? min(p.S_k, q_row + 1) : p.S_k;  // keys k0+k < lim are allowed
+            const int k0 = (j0 + as_my + j) * BN;
+            if (k0 < mask_lo || k0 + BN > mask_hi) {
 #pragma unroll
                 for (int k = 0; k < BN; ++k)
-                    if (k0 + k >= lim) s[k] = -INFINITY;
+                    if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
             }
             float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
             float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
@@ -415,17 +443,23 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
         }
         const bool row_ok = q_row < p.S_q;
-        if (ok && n_my > 0 && p.n_split == 1) {
+        if (ok && p.n_split == 1) {
             // ------------------------------------------------------------ epilogue: O = O_t / l
-            tc_fence_after();
-            const float inv_l = 1.0f / l;
+            // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
+            if (n_my > 0) tc_fence_after();
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
                             (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
                              static_cast<long long>(q_row) * p.o_ss) * 2;
             for (int cc = 0; cc < p.n_pv; cc += 16) {
                 uint32_t o[16];
-                tmem_ld16(o_addr + cc, o);
-                tmem_wait_ld();
+                if (n_my > 0) {
+                    tmem_ld16(o_addr + cc, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) o[k] = 0u;
+                }
                 if (!row_ok) continue;
                 uint32_t w[8];
 #pragma unroll
@@ -442,6 +476,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                         if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
                 }
             }
+            if (p.lse && row_ok)
+                p.lse[(static_cast<long long>(b) * p.H + h) * p.S_q + q_row] = lse_from(m_used, l);
         } else if (ok && p.n_split > 1) {
             // ------------------------------------------------------------ epilogue: partial O, m, l
             // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no

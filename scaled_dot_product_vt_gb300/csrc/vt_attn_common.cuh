@@ -14,6 +14,8 @@ constexpr int kMaxStages = 4;
 constexpr int kMaxSplit = 64;       // split-KV shares per work item, at most
 constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
 
+constexpr long long kBandInf = 1LL << 42;  // a band edge that no row reaches
+
 // Device status bits (the host maps them to vt_status codes).
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusBounds = 2u;
@@ -29,8 +31,13 @@ struct AttnParams {
     int v_chunks;     // 128-byte column chunks of a V row
     int n_pv;         // MMA N of P*V: D_v rounded up to 16
     int stages;
-    int causal;
+    // Allowed keys of query row i: [i + band_lo, i + band_hi] within [0, S_k); +-kBandInf stands
+    // for "no limit" (the host maps each mask kind to its band).
+    long long band_lo, band_hi;
+    int reverse_q;     // 1: launch the query blocks last-first (work grows with the block index)
+    int kv_group;      // query heads per key/value head: K/V head of query head h is h / kv_group
     float scale_log2;  // scale * log2(e)
+    float *lse;        // nullptr, or [B*H*S_q] natural-log log-sum-exp per row
     void *O;
     long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
     const void *V;               // read by the fp32 V loader
@@ -47,6 +54,33 @@ struct AttnParams {
     unsigned *status;  // device status word
 };
 
+
+// First allowed key of row r and one past its last, clamped to [0, S_k] (empty when lo >= hi).
+__device__ __forceinline__ int band_key_lo(const AttnParams &p, int r) {
+    const long long x = static_cast<long long>(r) + p.band_lo;
+    return static_cast<int>(x < 0 ? 0 : (x > p.S_k ? p.S_k : x));
+}
+__device__ __forceinline__ int band_key_hi(const AttnParams &p, int r) {
+    const long long x = static_cast<long long>(r) + p.band_hi + 1;
+    return static_cast<int>(x < 0 ? 0 : (x > p.S_k ? p.S_k : x));
+}
+
+// Key tiles [*a, *e) of `bn` keys that query rows first..last need (an empty range as 0, 0).
+__device__ __forceinline__ void band_tiles(const AttnParams &p, int first, int last, int bn, int *a, int *e) {
+    const int lo = band_key_lo(p, first), hi = band_key_hi(p, last);
+    if (lo < hi) {
+        *a = lo / bn;
+        *e = (hi + bn - 1) / bn;
+    } else {
+        *a = 0;
+        *e = 0;
+    }
+}
+
+// log(sum of exponentials) in natural-log units from a log2-unit reference max m and sum l.
+__device__ __forceinline__ float lse_from(float m, float l) {
+    return l > 0.0f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+}
 
 // Wait for the phase of `bar` with `parity`, giving up after the time limit or when
 // another role has aborted.  Returns false on give-up (after flagging the abort).

@@ -83,20 +83,19 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: all heads' heaviest causal query blocks first.
+    // Work item: all heads' heaviest query blocks first when work grows with the block index.
     const int bh_count = p.B * p.H;
     const int slot = blockIdx.x / bh_count;
     const int bh = blockIdx.x - slot * bh_count;
-    const int qb = p.causal ? (p.n_qblocks - 1 - slot) : slot;
+    const int qb = p.reverse_q ? (p.n_qblocks - 1 - slot) : slot;
     const int h = bh % p.H;
     const int b = bh / p.H;
+    const int hk = h / p.kv_group;  // key/value head
     const int q_row0 = qb * kBM;
-    const int n_ktiles_all = (p.S_k + BN - 1) / BN;
-    int n_kv = n_ktiles_all;
-    if (p.causal) {
-        const int last_row = min(q_row0 + kBM, p.S_q) - 1;
-        n_kv = min(n_kv, last_row / BN + 1);
-    }
+    // key tiles [j_first, j_first + n_kv) that some row of the block may see (none: n_kv = 0)
+    int j_first, j_end;
+    band_tiles(p, q_row0, min(q_row0 + kBM, p.S_q) - 1, BN, &j_first, &j_end);
+    const int n_kv = j_end - j_first;
 
     // Shared-memory carve-up (1024-byte aligned for the 128-byte swizzle).
     const uint32_t raw = smem_u32(smem_raw);
@@ -141,7 +140,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && n_kv > 0) {
             mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_bytes);
             for (int c = 0; c < p.q_chunks; ++c)
                 tma_load_4d(sQ + c * kBM * 128, &tmQ, smem_u32(&ctl.q_full), c * C::kChunkElems, q_row0, h, b);
@@ -152,13 +151,13 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 if (use > 0 && !wait_bounded(smem_u32(&ctl.empty[st]), (use - 1) & 1, ctl.abort_flag, p)) break;
                 mbar_arrive_expect_tx(smem_u32(&ctl.full_k[st]), k_bytes);
                 for (int c = 0; c < p.q_chunks; ++c)
-                    tma_load_4d(sK(st) + c * BN * 128, &tmK, smem_u32(&ctl.full_k[st]), c * C::kChunkElems, j * BN,
-                                h, b);
+                    tma_load_4d(sK(st) + c * BN * 128, &tmK, smem_u32(&ctl.full_k[st]), c * C::kChunkElems,
+                                (j_first + j) * BN, hk, b);
                 if (DT == kBF16) {
                     mbar_arrive_expect_tx(smem_u32(&ctl.full_v[st]), v_bytes);
                     for (int c = 0; c < p.v_chunks; ++c)
                         tma_load_4d(sV(st) + c * BN * 128, &tmV, smem_u32(&ctl.full_v[st]), c * C::kChunkElems,
-                                    j * BN, h, b);
+                                    (j_first + j) * BN, hk, b);
                 }
                 issued = j + 1;
             }
@@ -176,7 +175,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         // Descriptors are built once as (low, high) words and the K-steps are unrolled (KQ):
         // computing a descriptor per instruction would make this thread the bottleneck.
-        if (lane == 0) {
+        if (lane == 0 && n_kv > 0) {
             static_assert(DT == kF32, "this kernel serves fp32 I/O; bf16 uses the two-tile kernel");
             const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, 0);
@@ -233,7 +232,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         const int lt = threadIdx.x - 192;
         const int nd4 = p.n_pv / 4;  // 4-column groups, including the zero padding up to n_pv
         const float *vbh = static_cast<const float *>(p.V) + static_cast<long long>(b) * p.v_sb +
-                           static_cast<long long>(h) * p.v_sh;
+                           static_cast<long long>(hk) * p.v_sh;
         uint8_t *smem_gen = smem_raw + (base - raw);
         for (int j = 0; j < n_kv; ++j) {
             const int st = j % p.stages;
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 const int idx = lt + u * C::kVLoaders;
                 const int key = idx / nd4;
                 const int d0 = (idx - key * nd4) * 4;
-                const int kg = j * BN + key;
+                const int kg = (j_first + j) * BN + key;
                 val[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (idx < BN * nd4 && kg < p.S_k && d0 < p.D_v) {
                     const float *src = vbh + static_cast<long long>(kg) * p.v_ss + d0;
@@ -288,6 +287,11 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         const int q_row = q_row0 + row;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const float c = p.scale_log2;
+        // this row's allowed keys [key_lo, key_hi); a key tile starting below mask_lo or ending past
+        // mask_hi cuts some row's range and is masked (the same decision for the whole warpgroup)
+        const int key_lo = band_key_lo(p, q_row), key_hi = band_key_hi(p, q_row);
+        const int mask_lo = band_key_lo(p, min(q_row0 + kBM, p.S_q) - 1);
+        const int mask_hi = band_key_hi(p, q_row0);
         float m_used = -INFINITY;  // reference max (log2 units) of O and l
         float l = 0.0f;
         bool ok = true;
@@ -306,13 +310,11 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             float x[BN];
 #pragma unroll
             for (int k = 0; k < BN; ++k) x[k] = __uint_as_float(sr[k]) * c;
-            const int k0 = j * BN;
-            const bool need_mask = (k0 + BN > p.S_k) || (p.causal && k0 + BN - 1 > q_row0);
-            if (need_mask) {
-                const int lim = p.causal ? min(p.S_k, q_row + 1) : p.S_k;  // keys k0+k < lim are allowed
+            const int k0 = (j_first + j) * BN;
+            if (k0 < mask_lo || k0 + BN > mask_hi) {
 #pragma unroll
                 for (int k = 0; k < BN; ++k)
-                    if (k0 + k >= lim) x[k] = -INFINITY;
+                    if (k0 + k < key_lo || k0 + k >= key_hi) x[k] = -INFINITY;
             }
             float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
@@ -385,14 +387,15 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
         }
 
-        if (ok) {
+        if (ok && n_kv > 0) {
             ok = wait_bounded(smem_u32(&ctl.o_done), (n_kv - 1) & 1, ctl.abort_flag, p);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             // ------------------------------------------------------------ epilogue
-            tc_fence_after();
-            const float inv_l = 1.0f / l;
+            // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
+            if (n_kv > 0) tc_fence_after();
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             const uint32_t o_addr = tmem + lane_base + C::kColO;
             const bool row_ok = q_row < p.S_q;
             uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
@@ -400,8 +403,13 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                              static_cast<long long>(q_row) * p.o_ss) * C::kElt;
             for (int cc = 0; cc < p.n_pv; cc += 16) {
                 uint32_t o[16];
-                tmem_ld16(o_addr + cc, o);
-                tmem_wait_ld();
+                if (n_kv > 0) {
+                    tmem_ld16(o_addr + cc, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) o[k] = 0u;
+                }
                 if (!row_ok) continue;
                 float v[16];
 #pragma unroll
@@ -433,6 +441,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                     }
                 }
             }
+            if (p.lse && row_ok)
+                p.lse[(static_cast<long long>(b) * p.H + h) * p.S_q + q_row] = lse_from(m_used, l);
         }
     }
 

@@ -6,11 +6,12 @@
 // keeps every weight <= 1.  This is the continuation step of the coverage table's
 // attention_fwd_triton3 row (case 4 reads M, L and Out and merges a further key range), applied
 // to all shares at once.  HBM-bound: per row it reads n_split * (D_v + 2) floats and writes D_v.
+// The row's log-sum-exp, if asked for, is M + log2(L) in natural-log units.
 #pragma once
 
 #include <cstdint>
 
-#include "vt_ptx.cuh"
+#include "vt_attn_common.cuh"
 
 namespace vt {
 
@@ -19,6 +20,7 @@ struct MergeParams {
     const float *part_m;
     const float *part_l;
     void *O;
+    float *lse;      // nullptr, or one natural-log log-sum-exp per row
     long long rows;  // B * H * S_q
     int H, S_q, D_v, n_split;
     long long o_sb, o_sh, o_ss;
@@ -49,7 +51,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
             if (col < mp.D_v) acc[c] += w * po[col];
         }
     }
-    const float inv = 1.0f / L;
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;  // no share saw an allowed key: the row is 0
+    if (mp.lse && lane == 0) mp.lse[row] = lse_from(M, L);
     const long long i = row % mp.S_q;
     const long long bh = row / mp.S_q;
     const long long h = bh % mp.H, b = bh / mp.H;

@@ -138,6 +138,40 @@ class Workload:
     sigma_q: float
     sigma_kv: float
     seed: int
+    # Variants beyond plain/causal attention (empty mask: the modes in `causal` above).
+    H_kv: int = 0         # key/value heads (0: H)
+    mask: str = ""        # "none", "causal", "window" or "window_complement"
+    offset: int = 0
+    window: int = 0
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
+
+    def allowed_pairs(self) -> int:
+        """Number of (query, key) pairs the mask keeps in one (b, h) slice (mask set)."""
+        return int(self.keys_per_row().sum())
+
+    def keys_per_row(self) -> np.ndarray:
+        """|A_i| for every query row i of one (b, h) slice (mask set)."""
+        i = np.arange(self.S_q, dtype=np.int64)
+        hi = np.minimum(i + self.offset, self.S_k - 1)            # last key (causal kinds)
+        if self.mask == "none":
+            n = np.full(self.S_q, self.S_k, dtype=np.int64)
+        elif self.mask == "causal":
+            n = hi + 1
+        elif self.mask == "window":
+            lo = np.maximum(i + self.offset - self.window + 1, 0)
+            n = np.maximum(hi - lo + 1, 0)
+        elif self.mask == "window_complement":
+            n = np.maximum(np.minimum(i + self.offset - self.window, self.S_k - 1) + 1, 0)
+        else:
+            raise ValueError(f"unknown mask {self.mask!r}")
+        return n
+
+    def flops_masked(self) -> float:
+        """Algorithmic flops of a masked workload: 2*(D_qk+D_v) per kept (query, key) pair."""
+        return 2.0 * self.B * self.H * self.allowed_pairs() * (self.D_qk + self.D_v)
 
     @property
     def scale(self) -> float:
@@ -152,8 +186,8 @@ class Workload:
     def bytes(self) -> int:
         """Algorithmic bytes: Q, K, V read once and O written once."""
         elt = 2 if self.dtype == "bf16" else 4
-        return self.B * self.H * (self.S_q * self.D_qk + self.S_k * self.D_qk
-                                  + self.S_k * self.D_v + self.S_q * self.D_v) * elt
+        return self.B * (self.H * self.S_q * (self.D_qk + self.D_v)
+                         + self.kv_heads * self.S_k * (self.D_qk + self.D_v)) * elt
 
 
 # The five attention workloads: shapes, value distributions and seeds.
@@ -163,6 +197,13 @@ WORKLOADS = {
     "bf16_causal_2k": Workload("bf16_causal_2k", 4, 16, 2048, 2048, 128, 128, "bf16", (True,), "normal", 1.0, 1.0, 2),
     "bf16_ragged": Workload("bf16_ragged", 2, 32, 333, 8191, 96, 64, "bf16", (False,), "normal", 1.0, 1.0, 3),
     "bf16_causal_8k_peaky": Workload("bf16_causal_8k_peaky", 8, 16, 8192, 8192, 128, 128, "bf16", (True,), "normal", 4.0, 1.0, 4),
+    # masked and grouped-head variants (flops count the kept (query, key) pairs exactly)
+    "bf16_gqa_causal_8k": Workload("bf16_gqa_causal_8k", 4, 32, 8192, 8192, 128, 128, "bf16", (True,), "normal",
+                                   1.0, 1.0, 5, H_kv=8, mask="causal"),
+    "bf16_prefill_on_cache_8k": Workload("bf16_prefill_on_cache_8k", 8, 16, 1024, 8192, 128, 128, "bf16", (True,),
+                                         "normal", 1.0, 1.0, 6, mask="causal", offset=7168),
+    "bf16_window_1k_8k": Workload("bf16_window_1k_8k", 8, 16, 8192, 8192, 128, 128, "bf16", (True,), "normal",
+                                  1.0, 1.0, 7, mask="window", window=1024),
 }
 
 
@@ -175,9 +216,11 @@ def element_counts(B, H, S_q, S_k, D_qk, D_v):
     return tuple(int(np.prod(s)) for s in tensor_shapes(B, H, S_q, S_k, D_qk, D_v))
 
 
-def make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype="bf16", dist="normal", sigma_q=1.0, sigma_kv=1.0, seed=0):
-    """Q, K, V as numpy arrays of shape [B,H,S,D] (bf16 as uint16 bits, f32 as float32)."""
-    sq, sk, sv, _ = tensor_shapes(B, H, S_q, S_k, D_qk, D_v)
+def make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype="bf16", dist="normal", sigma_q=1.0, sigma_kv=1.0, seed=0, H_kv=None):
+    """Q, K, V as numpy arrays of shape [B,H,S,D] (bf16 as uint16 bits, f32 as float32); with H_kv, K and V
+    have H_kv heads.  Filled in the order Q, K, V from one stream."""
+    sq, _, _, _ = tensor_shapes(B, H, S_q, S_k, D_qk, D_v)
+    _, sk, sv, _ = tensor_shapes(B, H_kv or H, S_q, S_k, D_qk, D_v)
     pos = 0
     out = []
     for shape, sigma in ((sq, sigma_q), (sk, sigma_kv), (sv, sigma_kv)):
@@ -189,4 +232,5 @@ def make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype="bf16", dist="normal", sigma_q=1.0
 
 
 def make_workload(w: Workload):
-    return make_qkv(w.B, w.H, w.S_q, w.S_k, w.D_qk, w.D_v, w.dtype, w.dist, w.sigma_q, w.sigma_kv, w.seed)
+    return make_qkv(w.B, w.H, w.S_q, w.S_k, w.D_qk, w.D_v, w.dtype, w.dist, w.sigma_q, w.sigma_kv, w.seed,
+                    H_kv=w.kv_heads)

@@ -129,3 +129,44 @@ def test_splitkv_choose_without_gpu(lib):
     # no device to query: falls back to no split
     assert vt.vt_attn_splitkv_choose(1, 8, 256, 32768, 0, vt.VT_BF16) == 1
     assert vt.vt_attn_splitkv_choose(1, 8, 256, 32768, 0, vt.VT_F32) == 1
+
+
+# ---------------------------------------------------------------- the general entry point
+
+def general_call(H=4, H_kv=2, kind=0, offset=0, window=0, reserved=0, lse=None, n_split=1, ws=None, ws_bytes=0,
+                 dtype=vt.VT_BF16, mask=True):
+    st = (H * 32, 32, 8)
+    skv = (H_kv * 32, 32, 8) if H_kv > 0 else st
+    m = vt.vt_attn_mask(kind, reserved, offset, window) if mask else None
+    return vt.vt_attn_fwd_general(A, st, 2 * A, skv, 3 * A, skv, 4 * A, st, lse, 1, H, H_kv, 4, 4, 8, 8, 0.5, dtype,
+                                  m, n_split, ws, ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_kv=0), 1), (dict(H_kv=-1), 1), (dict(H_kv=3), 1),       # H must be a multiple of H_kv
+    (dict(kind=4), 1), (dict(kind=-1), 1), (dict(reserved=1), 1),
+    (dict(kind=1, offset=-1), 1),
+    (dict(kind=2, window=0), 1), (dict(kind=3, window=-4), 1),
+    (dict(kind=1, offset=(1 << 40) + 1), 2), (dict(kind=2, window=(1 << 40) + 1), 2),
+    (dict(lse=8 * A + 2), 1),                                       # lse not 4-byte aligned
+    (dict(lse=A + 16), 1),                                          # lse overlaps Q
+    (dict(n_split=0), 1), (dict(n_split=65), 2),
+    (dict(n_split=2), 1),                                           # no workspace
+    (dict(n_split=2, ws=8 * A, ws_bytes=1 << 24, dtype=vt.VT_F32), 2),
+    (dict(n_split=2, ws=8 * A, ws_bytes=1 << 24, lse=8 * A + 64), 1),  # lse inside the workspace
+])
+def test_general_argument_errors(lib, kw, code):
+    assert general_call(**kw) == code
+
+
+def test_general_empty_problem_and_null_mask(lib):
+    st = (32, 32, 8)
+    assert vt.vt_attn_fwd_general(A, st, 2 * A, st, 3 * A, st, 4 * A, st, None, 1, 0, 1, 4, 4, 8, 8, 0.5,
+                                  vt.VT_BF16, None, 1, None, 0, None, None) == 0
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    # a valid call with mask NULL reaches the launch, which reports the missing GPU
+    assert general_call(mask=False) == 4
+    assert general_call(kind=3, offset=2, window=5, lse=16 * A) == 4
+    assert vt.vt_last_device_status(0) == 4
