@@ -8,6 +8,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -19,6 +20,10 @@
 namespace vt {
 
 __device__ unsigned g_status_word;  // device status bits (kStatusTimeout, kStatusBounds)
+
+// Work-unit counters of the persistent bf16 kernel: two words per slot, zero between launches (the
+// last CTA of a launch resets its slot).  Static, so no call allocates.
+__device__ unsigned g_sched[kSchedSlots * 2];
 
 // Scratch of vt_attn_fwd_splitkv_noalloc, for callers that cannot allocate device memory: a
 // fixed array that exists on every GPU that loads this library, for as long as the process runs.
@@ -58,6 +63,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     unsigned *status = nullptr;
+    unsigned *sched = nullptr;  // g_sched on this device
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_info_mu;
@@ -75,10 +81,12 @@ bool device_info(int dev, DeviceInfo *out) {
     std::lock_guard<std::mutex> lock(g_info_mu);
     DeviceInfo &d = g_info[dev];
     if (!d.ready) {
-        void *status_ptr = nullptr;
+        void *status_ptr = nullptr, *sched_ptr = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&sched_ptr, g_sched) != cudaSuccess) return false;
         d.status = static_cast<unsigned *>(status_ptr);
+        d.sched = static_cast<unsigned *>(sched_ptr);
         d.ready = true;
     }
     *out = d;
@@ -249,8 +257,13 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         const long long bh = B * H;
         long long grp = (2LL * sms + p.n_qblocks - 1) / p.n_qblocks;
         p.head_group = static_cast<int>(grp < 1 ? 1 : (grp > bh ? bh : grp));
-        const long long items = static_cast<long long>(p.n_qblocks) * bh * n_split;
-        if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        const long long units = static_cast<long long>(p.n_qblocks) * bh * n_split;
+        if (units > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        p.n_units = static_cast<int>(units);
+        static std::atomic<unsigned> launch_seq{0};
+        p.sched = info.sched + 2 * (launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+        // persistent: one CTA per SM (the shared memory admits one) draws units until none is left
+        const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
         // Q K^T K-steps of 16, rounded up to an even count (the TMA zero-fills past D_qk)
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
         void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
@@ -258,7 +271,7 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
                         : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4>
                                       : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6> : attn_fwd_bf16_2q_kernel<8>;
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
-        kern<<<static_cast<unsigned>(items), q2::kThreads, smem, stream>>>(tq, tk, tv, p);
+        kern<<<grid, q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
         if (n_split > 1) {
             MergeParams mp{};
@@ -301,6 +314,7 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         p.n_split = 1;  // split-KV is served by the bf16 kernel only
         const long long items = static_cast<long long>(p.n_qblocks) * B * H;
         if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        p.n_units = static_cast<int>(items);
         kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
         return VT_OK;

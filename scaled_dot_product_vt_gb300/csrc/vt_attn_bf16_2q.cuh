@@ -1,10 +1,17 @@
 // Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per CTA sharing every
 // 128-key K/V tile, one softmax warpgroup per query tile, single-thread tcgen05 issue.
 //
-// One CTA computes 256 query rows of one (b, h) slice as query tiles t = 0, 1 (rows
-// r0 + 128 t .. r0 + 128 t + 127).  Warp roles (12 warps, three warpgroups):
-//   warp 0       TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ... through a ring of
-//                equal shared-memory slots (mbarrier full/empty per slot).
+// Persistent: one CTA per SM takes work units in launch order from a global counter (the
+// producer warp draws them and passes them to the other roles through a small ring in shared
+// memory), so the heavy units that come first spread over the SMs as they free up.
+// A unit is 256 query rows of one (b, h) slice, as query tiles t = 0, 1 (rows r0 + 128 t ..
+// r0 + 128 t + 127), and one share of their key tiles.  TMEM, barriers and descriptors live
+// for the whole CTA; every barrier's phase is counted across units, so the producer loads the
+// next unit's Q and K/V while the current unit's last tiles and epilogue run.
+// Warp roles (12 warps, three warpgroups):
+//   warp 0       TMA producer: per unit the Q tiles that have work (once the previous unit's last
+//                Q K^T has read Q), then K_0, V_0, K_1, V_1, ... through a ring of equal
+//                shared-memory slots (mbarrier full/empty per slot) that runs on across units.
 //   warp 1       TMEM owner and MMA issuer (one thread).  Per key tile j the tensor core runs
 //                  O_0 += P_0,j V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1,j V_j,  S_1 = Q_1 K_{j+1}^T
 //                so while softmax warpgroup t works on S_t, the tensor core works for the other
@@ -14,12 +21,14 @@
 //   warps 2-3    idle (they complete warpgroup 0, which gives registers to the softmax warpgroups)
 //   warps 4-7    softmax warpgroup of tile 0, one row per thread (TMEM lane quadrant = warp % 4)
 //   warps 8-11   softmax warpgroup of tile 1
-// Registers: launched at 168 per thread; warpgroup 0 shrinks to 56 and the softmax warpgroups
-// grow to 224 (128 x 56 + 256 x 224 = 384 x 168, so the increase never waits on a shortfall).
+// Registers: launched at 168 per thread; warpgroup 0 shrinks to 72 and the softmax warpgroups
+// grow to 216 (128 x 72 + 256 x 216 = 384 x 168, so the increase never waits on a shortfall).
 // TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.  P_t,j overwrites S_t,j as bf16
 // pairs (64 columns) and is read from TMEM by the P V product.  A commit after S_t = Q_t K^T
 // also covers the P V issued before it, so when softmax t sees its next scores, O_t is final
-// for the previous tile and may be rescaled in place.
+// for the previous tile and may be rescaled in place.  Softmax t reads O_t for a unit's epilogue
+// before it hands over the next unit's first P_t, and the first P_t V of a unit (which overwrites
+// O_t) waits for that hand-over: no separate barrier guards O_t between units.
 //
 // The decomposition (query block, head, batch), the tail masks and the write set follow the
 // FA-1 boundary kernel verified on the VeriTile page "VeriTile.Examples.FlashAttention1.
@@ -35,10 +44,12 @@ namespace q2 {
 constexpr int kBN = 128;            // keys per tile
 constexpr int kRows = 256;          // query rows per CTA
 constexpr int kThreads = 384;       // 12 warps
-constexpr int kRegsControl = 64;    // warpgroup 0 after setmaxnreg
+constexpr int kRegsControl = 72;    // warpgroup 0 after setmaxnreg
 constexpr int kRegsSoftmax = 216;   // softmax warpgroups after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch");
 constexpr int kMaxSlots = 6;
+constexpr int kUnitRing = 4;        // unit indices in flight between the producer and the other roles
+constexpr int kUnitReaders = 1 + 8;  // the MMA thread and one lane of each softmax warp
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunk = 64;          // bf16 elements per 128-byte chunk
 constexpr uint32_t kChunkBytes = kBN * 128;  // one 128-byte column chunk of a 128-row tile
@@ -55,9 +66,13 @@ struct Ctl {
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
     uint64_t q_full;
+    uint64_t q_empty;     // the unit's last Q K^T has read Q (the next unit's Q may be loaded)
     uint64_t s_full[2];   // scores of tile t ready (and every earlier MMA done)
     uint64_t p_full[2];   // P of tile t written (128 arrivals)
     uint64_t o_done[2];   // last P V of tile t done
+    uint64_t unit_full[kUnitRing];   // unit index k written by the producer
+    uint64_t unit_empty[kUnitRing];  // unit index k read by every other role
+    int unit_id[kUnitRing];          // the unit, or -1 once the counter is exhausted
     uint64_t drain;
     uint64_t stall;
     uint32_t tmem_base;
@@ -68,6 +83,79 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// One work unit: a 256-row query block of one (b, h) and one share of its key tiles.
+struct Unit {
+    int b, h, hk, r0;
+    int j0, n_kv;             // the share's first key tile and its number of key tiles
+    int as0, es0, as1, es1;   // key tiles [as_t, es_t) of the share that query tile t needs
+};
+
+// Units run over groups of `head_group` heads; inside a group, the heaviest query blocks first
+// when work grows with the block index; the shares of one block are adjacent.
+__device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
+    Unit U;
+    const int split = u % p.n_split;
+    const int item = u / p.n_split;
+    const int BH = p.B * p.H;
+    const int per_group = p.head_group * p.n_qblocks;
+    const int g = item / per_group;
+    const int rr = item - g * per_group;
+    const int g_heads = min(p.head_group, BH - g * p.head_group);
+    const int slot_q = rr / g_heads;
+    const int bh = g * p.head_group + (rr - slot_q * g_heads);
+    const int qb = p.reverse_q ? (p.n_qblocks - 1 - slot_q) : slot_q;
+    U.h = bh % p.H;
+    U.b = bh / p.H;
+    U.hk = U.h / p.kv_group;
+    U.r0 = qb * kRows;
+    // The union of both query tiles' key-tile ranges is contiguous (tile 1's first key never lies
+    // past tile 0's last); it is cut into n_split contiguous shares.
+    int a[2], e[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int first = U.r0 + t * kBM;
+        if (first >= p.S_q) {
+            a[t] = 0;
+            e[t] = 0;
+        } else {
+            band_tiles(p, first, min(first + kBM, p.S_q) - 1, kBN, &a[t], &e[t]);
+        }
+    }
+    const bool has0 = e[0] > a[0], has1 = e[1] > a[1];
+    const int A = has0 ? (has1 ? min(a[0], a[1]) : a[0]) : (has1 ? a[1] : 0);
+    const int E = has0 ? (has1 ? max(e[0], e[1]) : e[0]) : (has1 ? e[1] : 0);
+    const int n_item = E - A;
+    const int per = (n_item + p.n_split - 1) / p.n_split;
+    const int lo = min(split * per, n_item), hi = min(n_item, lo + per);
+    U.j0 = A + lo;
+    U.n_kv = hi - lo;
+    int as[2], es[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        as[t] = min(max(a[t] - U.j0, 0), U.n_kv);
+        es[t] = min(max(e[t] - U.j0, 0), U.n_kv);
+        if (es[t] <= as[t]) {
+            as[t] = 0;
+            es[t] = 0;
+        }
+    }
+    U.as0 = as[0];
+    U.es0 = es[0];
+    U.as1 = as[1];
+    U.es1 = es[1];
+    return U;
+}
+
+// The n-th unit this CTA works on, as the producer published it (-1: no more units); false on
+// abort.  Every reader calls it once per n, in order, and releases the ring entry.
+__device__ __forceinline__ bool next_unit(Ctl &ctl, int n, int *u, const AttnParams &p) {
+    const int k = n % kUnitRing;
+    if (!wait_bounded(smem_u32(&ctl.unit_full[k]), (n / kUnitRing) & 1, ctl.abort_flag, p)) return false;
+    *u = *reinterpret_cast<volatile int *>(&ctl.unit_id[k]);
+    mbar_arrive(smem_u32(&ctl.unit_empty[k]));
+    return true;
 }
 
 }  // namespace q2
@@ -85,62 +173,6 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- work item: groups of `head_group` heads; inside a group, heavy causal blocks first;
-    // the splits of one item are adjacent in the launch order
-    const int split = blockIdx.x % p.n_split;
-    const int item = blockIdx.x / p.n_split;
-    const int BH = p.B * p.H;
-    const int per_group = p.head_group * p.n_qblocks;
-    const int g = item / per_group;
-    const int rr = item - g * per_group;
-    const int g_heads = min(p.head_group, BH - g * p.head_group);
-    const int slot_q = rr / g_heads;
-    const int bh = g * p.head_group + (rr - slot_q * g_heads);
-    const int qb = p.reverse_q ? (p.n_qblocks - 1 - slot_q) : slot_q;
-    const int h = bh % p.H;
-    const int b = bh / p.H;
-    const int hk = h / p.kv_group;  // key/value head
-    const int r0 = qb * kRows;
-
-    // Key tiles of this CTA: the union of both query tiles' ranges (contiguous: tile 1's first key
-    // never lies past tile 0's last), cut into n_split contiguous shares.  [as_t, es_t) is the part
-    // query tile t needs, relative to the share's first tile j0 (empty as 0, 0).
-    int as0, es0, as1, es1, j0, n_kv;
-    {
-        int a[2], e[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const int first = r0 + t * kBM;
-            if (first >= p.S_q) {
-                a[t] = 0;
-                e[t] = 0;
-            } else {
-                band_tiles(p, first, min(first + kBM, p.S_q) - 1, BN, &a[t], &e[t]);
-            }
-        }
-        const bool has0 = e[0] > a[0], has1 = e[1] > a[1];
-        const int A = has0 ? (has1 ? min(a[0], a[1]) : a[0]) : (has1 ? a[1] : 0);
-        const int E = has0 ? (has1 ? max(e[0], e[1]) : e[0]) : (has1 ? e[1] : 0);
-        const int n_item = E - A;
-        const int per = (n_item + p.n_split - 1) / p.n_split;
-        const int lo = min(split * per, n_item), hi = min(n_item, lo + per);
-        j0 = A + lo;
-        n_kv = hi - lo;
-        int as[2], es[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            as[t] = min(max(a[t] - j0, 0), n_kv);
-            es[t] = min(max(e[t] - j0, 0), n_kv);
-            if (es[t] <= as[t]) {
-                as[t] = 0;
-                es[t] = 0;
-            }
-        }
-        as0 = as[0];
-        es0 = es[0];
-        as1 = as[1];
-        es1 = es[1];
-    }
     const int n_slots = p.stages;
 
     // ---- shared memory: Q tile 0, Q tile 1, then `n_slots` equal K/V slots
@@ -159,10 +191,15 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             mbar_init(smem_u32(&ctl.empty[s]), 1);
         }
         mbar_init(smem_u32(&ctl.q_full), 1);
+        mbar_init(smem_u32(&ctl.q_empty), 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&ctl.s_full[t]), 1);
             mbar_init(smem_u32(&ctl.p_full[t]), 128);
             mbar_init(smem_u32(&ctl.o_done[t]), 1);
+        }
+        for (int k = 0; k < kUnitRing; ++k) {
+            mbar_init(smem_u32(&ctl.unit_full[k]), 1);
+            mbar_init(smem_u32(&ctl.unit_empty[k]), kUnitReaders);
         }
         mbar_init(smem_u32(&ctl.drain), 1);
         mbar_init(smem_u32(&ctl.stall), 1);
@@ -187,52 +224,73 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_kv > 0) {
-            const bool load0 = es0 > as0, load1 = es1 > as1;  // Q tiles with work in this share
-            mbar_arrive_expect_tx(smem_u32(&ctl.q_full), (int(load0) + int(load1)) * q_tile_bytes);
-            if (load0)
-                for (int c = 0; c < p.q_chunks; ++c)
-                    tma_load_4d(sQ0 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0, h, b);
-            if (load1)
-                for (int c = 0; c < p.q_chunks; ++c)
-                    tma_load_4d(sQ1 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, r0 + kBM, h, b);
-            // loads i = 2j (K_j) and 2j + 1 (V_j) go to slot i mod n_slots
+        if (lane == 0) {
+            // loads i = 2j (K_j) and 2j + 1 (V_j) of a unit go to the ring's next slots
             int s = 0;
             uint32_t empty_phase = 0;  // bit s: parity of the next empty-phase of slot s to wait for
-            int loads = 0;
+            int loads = 0, q_loads = 0;
             bool ok = true;
-            for (int i = 0; ok && i < 2 * n_kv; ++i) {
-                if (loads >= n_slots) {
-                    ok = wait_bounded(smem_u32(&ctl.empty[s]), (empty_phase >> s) & 1u, ctl.abort_flag, p);
-                    empty_phase ^= 1u << s;
+            for (int n = 0; ok; ++n) {
+                // draw the next unit and publish it to the other roles
+                const int k = n % kUnitRing;
+                if (n >= kUnitRing) {
+                    ok = wait_bounded(smem_u32(&ctl.unit_empty[k]), ((n / kUnitRing) - 1) & 1, ctl.abort_flag, p);
                     if (!ok) break;
                 }
-                const uint32_t dst = sSlot0 + s * slot_bytes;
-                const uint32_t bar = smem_u32(&ctl.full[s]);
-                const int j = i >> 1;
-                if ((i & 1) == 0) {
-                    mbar_arrive_expect_tx(bar, k_bytes);
-                    for (int c = 0; c < p.q_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, (j0 + j) * BN, hk, b);
-                } else {
-                    mbar_arrive_expect_tx(bar, v_bytes);
-                    for (int c = 0; c < p.v_chunks; ++c)
-                        tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, (j0 + j) * BN, hk, b);
+                const unsigned drawn = atomicAdd(&p.sched[0], 1u);
+                const int u = drawn < static_cast<unsigned>(p.n_units) ? static_cast<int>(drawn) : -1;
+                *reinterpret_cast<volatile int *>(&ctl.unit_id[k]) = u;
+                mbar_arrive(smem_u32(&ctl.unit_full[k]));
+                if (u < 0) break;
+                const Unit U = decode_unit(p, u);
+                if (U.n_kv == 0) continue;
+                if (q_loads > 0) {  // the previous unit's last Q K^T has read Q
+                    ok = wait_bounded(smem_u32(&ctl.q_empty), (q_loads - 1) & 1, ctl.abort_flag, p);
+                    if (!ok) break;
                 }
-                ++loads;
-                if (++s == n_slots) s = 0;
+                const bool load0 = U.es0 > U.as0, load1 = U.es1 > U.as1;  // Q tiles with work
+                mbar_arrive_expect_tx(smem_u32(&ctl.q_full), (int(load0) + int(load1)) * q_tile_bytes);
+                if (load0)
+                    for (int c = 0; c < p.q_chunks; ++c)
+                        tma_load_4d(sQ0 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, U.r0, U.h, U.b);
+                if (load1)
+                    for (int c = 0; c < p.q_chunks; ++c)
+                        tma_load_4d(sQ1 + c * kChunkBytes, &tmQ, smem_u32(&ctl.q_full), c * kChunk, U.r0 + kBM, U.h,
+                                    U.b);
+                ++q_loads;
+                for (int i = 0; i < 2 * U.n_kv; ++i) {
+                    if (loads >= n_slots) {
+                        ok = wait_bounded(smem_u32(&ctl.empty[s]), (empty_phase >> s) & 1u, ctl.abort_flag, p);
+                        empty_phase ^= 1u << s;
+                        if (!ok) break;
+                    }
+                    const uint32_t dst = sSlot0 + s * slot_bytes;
+                    const uint32_t bar = smem_u32(&ctl.full[s]);
+                    const int j = i >> 1;
+                    if ((i & 1) == 0) {
+                        mbar_arrive_expect_tx(bar, k_bytes);
+                        for (int c = 0; c < p.q_chunks; ++c)
+                            tma_load_4d(dst + c * kChunkBytes, &tmK, bar, c * kChunk, (U.j0 + j) * BN, U.hk, U.b);
+                    } else {
+                        mbar_arrive_expect_tx(bar, v_bytes);
+                        for (int c = 0; c < p.v_chunks; ++c)
+                            tma_load_4d(dst + c * kChunkBytes, &tmV, bar, c * kChunk, (U.j0 + j) * BN, U.hk, U.b);
+                    }
+                    ++loads;
+                    if (++s == n_slots) s = 0;
+                }
             }
             if (ctl.abort_flag) {
-                // Let every copy this thread started land before the CTA's memory goes away:
-                // the last min(loads, n_slots) loads, one per slot, each on the full phase it used.
-                wait_drain(smem_u32(&ctl.q_full), 0, p);
+                // Let every copy this thread started land before the CTA's memory goes away: the
+                // last Q load and the last min(loads, n_slots) slot loads, each on the phase it used.
+                if (q_loads > 0) wait_drain(smem_u32(&ctl.q_full), (q_loads - 1) & 1, p);
                 for (int k = max(0, loads - n_slots); k < loads; ++k)
                     wait_drain(smem_u32(&ctl.full[k % n_slots]), (k / n_slots) & 1, p);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0) {
             const uint32_t idesc_qk = instr_desc(1, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(1, kBM, p.n_pv, 1);
             // Descriptors as (low, high) words: offsets only move the low word (start address >> 4).
@@ -249,6 +307,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             const uint32_t o_col0 = tmem + col_o(0), o_col1 = tmem + col_o(1);
             bool ok = true, any_mma = false;
             uint32_t full_phase = 0;  // bit s: parity of the next full-phase of slot s
+            uint32_t p_par0 = 0, p_par1 = 0;  // parity of the next P hand-over of tile 0 / 1
+            uint32_t q_par = 0;               // parity of the next Q load
 
             // K/V slots are filled by TMA: the mbarrier's completed transaction count already makes
             // the bytes visible to the tensor core, so no tcgen05 fence is needed after this wait.
@@ -271,58 +331,71 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             };
 
             if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook
-            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
-            // query tile t takes part in key tile j when as_t <= j < es_t
-            auto act0 = [&](int j) { return j >= as0 && j < es0; };
-            auto act1 = [&](int j) { return j >= as1 && j < es1; };
-            int ks = 0;  // slot of K_j
-            if (ok) ok = wait_full(ks);
-            if (ok) {
-                const uint32_t k_lo = k_lo0 + ks * slot_step;
-                if (act0(0)) {
-                    qk(s_col0, q_lo0, k_lo);
-                    mma_commit(smem_u32(&ctl.s_full[0]));
+            int ks = 0;  // slot of the next K tile (the ring runs on across units)
+            for (int n = 0; ok; ++n) {
+                int u;
+                if (!(ok = next_unit(ctl, n, &u, p)) || u < 0) break;
+                const Unit U = decode_unit(p, u);
+                const int n_kv = U.n_kv;
+                if (n_kv == 0) continue;
+                const int as0 = U.as0, es0 = U.es0, as1 = U.as1, es1 = U.es1;
+                // query tile t takes part in key tile j when as_t <= j < es_t
+                auto act0 = [&](int j) { return j >= as0 && j < es0; };
+                auto act1 = [&](int j) { return j >= as1 && j < es1; };
+                if (!(ok = wait_bounded(smem_u32(&ctl.q_full), q_par, ctl.abort_flag, p))) break;
+                q_par ^= 1u;
+                if (!(ok = wait_full(ks))) break;
+                {
+                    const uint32_t k_lo = k_lo0 + ks * slot_step;
+                    if (act0(0)) {
+                        qk(s_col0, q_lo0, k_lo);
+                        mma_commit(smem_u32(&ctl.s_full[0]));
+                    }
+                    if (act1(0)) {
+                        qk(s_col1, q_lo1, k_lo);
+                        mma_commit(smem_u32(&ctl.s_full[1]));
+                    }
+                    if (n_kv == 1) mma_commit(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
+                    mma_commit(smem_u32(&ctl.empty[ks]));
+                    any_mma = true;
                 }
-                if (act1(0)) {
-                    qk(s_col1, q_lo1, k_lo);
-                    mma_commit(smem_u32(&ctl.s_full[1]));
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int vs = ks + 1 == n_slots ? 0 : ks + 1;  // slot of V_j
+                    const int kn = vs + 1 == n_slots ? 0 : vs + 1;  // slot of K_{j+1} (or the next unit's K_0)
+                    const bool more = j + 1 < n_kv;
+                    if (!(ok = wait_full(vs))) break;
+                    const uint32_t v_lo = v_lo0 + vs * slot_step;
+                    const uint32_t kn_lo = k_lo0 + kn * slot_step;
+                    if (act0(j)) {
+                        if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), p_par0, ctl.abort_flag, p))) break;
+                        p_par0 ^= 1u;
+                        tc_fence_after();
+                        pv(o_col0, s_col0, v_lo, j > as0);
+                    }
+                    if (more && !(ok = wait_full(kn))) break;
+                    if (act0(j + 1)) {
+                        qk(s_col0, q_lo0, kn_lo);
+                        mma_commit(smem_u32(&ctl.s_full[0]));
+                    } else if (act0(j)) {
+                        mma_commit(smem_u32(&ctl.o_done[0]));
+                    }
+                    if (act1(j)) {
+                        if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), p_par1, ctl.abort_flag, p))) break;
+                        p_par1 ^= 1u;
+                        tc_fence_after();
+                        pv(o_col1, s_col1, v_lo, j > as1);
+                    }
+                    mma_commit(smem_u32(&ctl.empty[vs]));
+                    if (act1(j + 1)) {
+                        qk(s_col1, q_lo1, kn_lo);
+                        mma_commit(smem_u32(&ctl.s_full[1]));
+                    } else if (act1(j)) {
+                        mma_commit(smem_u32(&ctl.o_done[1]));
+                    }
+                    if (j + 2 == n_kv) mma_commit(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
+                    if (more) mma_commit(smem_u32(&ctl.empty[kn]));
+                    ks = kn;
                 }
-                mma_commit(smem_u32(&ctl.empty[ks]));
-                any_mma = true;
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int vs = ks + 1 == n_slots ? 0 : ks + 1;  // slot of V_j
-                const int kn = vs + 1 == n_slots ? 0 : vs + 1;  // slot of K_{j+1}
-                const bool more = j + 1 < n_kv;
-                if (!(ok = wait_full(vs))) break;
-                const uint32_t v_lo = v_lo0 + vs * slot_step;
-                const uint32_t kn_lo = k_lo0 + kn * slot_step;
-                if (act0(j)) {
-                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), (j - as0) & 1, ctl.abort_flag, p))) break;
-                    tc_fence_after();
-                    pv(o_col0, s_col0, v_lo, j > as0);
-                }
-                if (more && !(ok = wait_full(kn))) break;
-                if (act0(j + 1)) {
-                    qk(s_col0, q_lo0, kn_lo);
-                    mma_commit(smem_u32(&ctl.s_full[0]));
-                } else if (act0(j)) {
-                    mma_commit(smem_u32(&ctl.o_done[0]));
-                }
-                if (act1(j)) {
-                    if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), (j - as1) & 1, ctl.abort_flag, p))) break;
-                    tc_fence_after();
-                    pv(o_col1, s_col1, v_lo, j > as1);
-                }
-                mma_commit(smem_u32(&ctl.empty[vs]));
-                if (act1(j + 1)) {
-                    qk(s_col1, q_lo1, kn_lo);
-                    mma_commit(smem_u32(&ctl.s_full[1]));
-                } else if (act1(j)) {
-                    mma_commit(smem_u32(&ctl.o_done[1]));
-                }
-                if (more) mma_commit(smem_u32(&ctl.empty[kn]));
-                ks = kn;
             }
             if (!ok && any_mma) {
                 mma_commit(smem_u32(&ctl.drain));
@@ -336,15 +409,6 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         const int t = (warp - 4) >> 2;              // query tile of this warpgroup
         const int quad = warp & 3;                  // TMEM lane quadrant
         const int row = quad * 32 + lane;
-        const int tile_row0 = r0 + t * kBM;
-        const int q_row = tile_row0 + row;
-        const int as_my = t ? as1 : as0;
-        const int n_my = (t ? es1 : es0) - as_my;
-        // this row's allowed keys [key_lo, key_hi); a key tile starting below mask_lo or ending past
-        // mask_hi cuts some row's range and is masked (the same decision for the whole warpgroup)
-        const int key_lo = band_key_lo(p, q_row), key_hi = band_key_hi(p, q_row);
-        const int mask_lo = band_key_lo(p, min(tile_row0 + kBM, p.S_q) - 1);
-        const int mask_hi = band_key_hi(p, tile_row0);
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + col_s(t);
         const uint32_t o_addr = tmem + lane_base + col_o(t);
@@ -352,165 +416,187 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         const bool fold = p.scale_log2 > 0.0f;
         const float c = fold ? p.scale_log2 : 1.0f;
         const float2 c2 = make_float2(c, c);
-        float m_used = -INFINITY;  // reference max (log2 units) of O_t and l
-        float l = 0.0f;
+        uint32_t s_par = 0, o_par = 0;  // parities of the next scores and the next o_done of this tile
         bool ok = true;
 
-        for (int j = 0; j < n_my; ++j) {
-            ok = wait_bounded(smem_u32(&ctl.s_full[t]), j & 1, ctl.abort_flag, p);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[BN];
-#pragma unroll
-            for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
-            tmem_wait_ld();
-            float s[BN];
-#pragma unroll
-            for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
-            if (!fold) {
-#pragma unroll
-                for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
-            }
-            const int k0 = (j0 + as_my + j) * BN;
-            if (k0 < mask_lo || k0 + BN > mask_hi) {
-#pragma unroll
-                for (int k = 0; k < BN; ++k)
-                    if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
-            }
-            float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-            float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-            for (int k = 12; k < BN - 4; k += 8) {
-                mx0 = fmax3(mx0, s[k], s[k + 1]);
-                mx1 = fmax3(mx1, s[k + 2], s[k + 3]);
-                mx2 = fmax3(mx2, s[k + 4], s[k + 5]);
-                mx3 = fmax3(mx3, s[k + 6], s[k + 7]);
-            }
-            mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
-            mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-            const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;  // c > 0: -inf stays -inf
-            const float m_new = fmaxf(m_used, m_tile);
-            // Lazy rescale: keep the old reference unless the max grew by more than tau.
-            const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kTau);
-            float alpha = 1.0f;
-            if (resc) {
-                alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);
-                l *= alpha;
-                m_used = m_new;
-            }
-            const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-            // P_t,j over S_t,j (bf16 pairs): each 32-score chunk goes to TMEM as 16 columns as
-            // soon as it is exponentiated, which keeps the live registers near the 128 scores.
-#pragma unroll
-            for (int cc = 0; cc < BN; cc += 32) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const float2 x0 = __ffma2_rn(make_float2(s[cc + k], s[cc + k + 1]), c2, nm2);
-                    const float2 x1 = __ffma2_rn(make_float2(s[cc + k + 2], s[cc + k + 3]), c2, nm2);
-                    const float2 e0 = make_float2(ex2(x0.x), ex2(x0.y));
-                    const float2 e1 = make_float2(ex2(x1.x), ex2(x1.y));
-                    acc0 = __fadd2_rn(acc0, e0);
-                    acc1 = __fadd2_rn(acc1, e1);
-                    pk[k / 2] = pack_bf16x2(e0.x, e0.y);
-                    pk[k / 2 + 1] = pack_bf16x2(e1.x, e1.y);
-                }
-                tmem_st16(s_addr + cc / 2, pk);
-            }
-            l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-            // O_t *= alpha where the reference moved (after the scores are dead, to keep registers low).  The scores just read were committed after
-            // P_t,j-1 V_j-1, so O_t holds its final value for tile j-1 and no MMA touches it now.
-            if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                for (int cc = 0; cc < p.n_pv; cc += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(o_addr + cc, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tmem_st32(o_addr + cc, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&ctl.p_full[t]));
-        }
+        for (int n = 0; ok; ++n) {
+            int u = -1;
+            if (lane == 0) ok = next_unit(ctl, n, &u, p);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (!ok || u < 0) break;
+            const Unit U = decode_unit(p, u);
+            const int tile_row0 = U.r0 + t * kBM;
+            const int q_row = tile_row0 + row;
+            const int as_my = t ? U.as1 : U.as0;
+            const int n_my = (t ? U.es1 : U.es0) - as_my;
+            // this row's allowed keys [key_lo, key_hi); a key tile starting below mask_lo or ending past
+            // mask_hi cuts some row's range and is masked (the same decision for the whole warpgroup)
+            const int key_lo = band_key_lo(p, q_row), key_hi = band_key_hi(p, q_row);
+            const int mask_lo = band_key_lo(p, min(tile_row0 + kBM, p.S_q) - 1);
+            const int mask_hi = band_key_hi(p, tile_row0);
+            float m_used = -INFINITY;  // reference max (log2 units) of O_t and l
+            float l = 0.0f;
 
-        if (ok && n_my > 0) {
-            ok = wait_bounded(smem_u32(&ctl.o_done[t]), 0, ctl.abort_flag, p);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        const bool row_ok = q_row < p.S_q;
-        if (ok && p.n_split == 1) {
-            // ------------------------------------------------------------ epilogue: O = O_t / l
-            // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
-            if (n_my > 0) tc_fence_after();
-            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
-                            (static_cast<long long>(b) * p.o_sb + static_cast<long long>(h) * p.o_sh +
-                             static_cast<long long>(q_row) * p.o_ss) * 2;
-            for (int cc = 0; cc < p.n_pv; cc += 16) {
-                uint32_t o[16];
-                if (n_my > 0) {
-                    tmem_ld16(o_addr + cc, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k] = 0u;
+            for (int j = 0; j < n_my; ++j) {
+                ok = wait_bounded(smem_u32(&ctl.s_full[t]), s_par, ctl.abort_flag, p);
+                s_par ^= 1u;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sr[BN];
+                #pragma unroll
+                for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
+                tmem_wait_ld();
+                float s[BN];
+                #pragma unroll
+                for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
+                if (!fold) {
+                    #pragma unroll
+                    for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
                 }
-                if (!row_ok) continue;
-                uint32_t w[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-                if (cc + 16 <= p.D_v) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
-                    uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                const int k0 = (U.j0 + as_my + j) * BN;
+                if (k0 < mask_lo || k0 + BN > mask_hi) {
+                    #pragma unroll
+                    for (int k = 0; k < BN; ++k)
+                        if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
                 }
+                float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+                float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+                #pragma unroll
+                for (int k = 12; k < BN - 4; k += 8) {
+                    mx0 = fmax3(mx0, s[k], s[k + 1]);
+                    mx1 = fmax3(mx1, s[k + 2], s[k + 3]);
+                    mx2 = fmax3(mx2, s[k + 4], s[k + 5]);
+                    mx3 = fmax3(mx3, s[k + 6], s[k + 7]);
+                }
+                mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+                mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;  // c > 0: -inf stays -inf
+                const float m_new = fmaxf(m_used, m_tile);
+                // Lazy rescale: keep the old reference unless the max grew by more than tau.
+                const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kTau);
+                float alpha = 1.0f;
+                if (resc) {
+                    alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
+                const float2 nm2 = make_float2(-m_ref, -m_ref);
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
+                // P_t,j over S_t,j (bf16 pairs): each 32-score chunk goes to TMEM as 16 columns as
+                // soon as it is exponentiated, which keeps the live registers near the 128 scores.
+                #pragma unroll
+                for (int cc = 0; cc < BN; cc += 32) {
+                    uint32_t pk[16];
+                    #pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        const float2 x0 = __ffma2_rn(make_float2(s[cc + k], s[cc + k + 1]), c2, nm2);
+                        const float2 x1 = __ffma2_rn(make_float2(s[cc + k + 2], s[cc + k + 3]), c2, nm2);
+                        const float2 e0 = make_float2(ex2(x0.x), ex2(x0.y));
+                        const float2 e1 = make_float2(ex2(x1.x), ex2(x1.y));
+                        acc0 = __fadd2_rn(acc0, e0);
+                        acc1 = __fadd2_rn(acc1, e1);
+                        pk[k / 2] = pack_bf16x2(e0.x, e0.y);
+                        pk[k / 2 + 1] = pack_bf16x2(e1.x, e1.y);
+                    }
+                    tmem_st16(s_addr + cc / 2, pk);
+                }
+                l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+                // O_t *= alpha where the reference moved (after the scores are dead, to keep registers
+                // low).  The scores just read were committed after P_t,j-1 V_j-1, so O_t holds its final
+                // value for tile j-1 and no MMA touches it now.
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                    for (int cc = 0; cc < p.n_pv; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + cc, o);
+                        tmem_wait_ld();
+                        #pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tmem_st32(o_addr + cc, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ctl.p_full[t]));
             }
-            if (p.lse && row_ok)
-                p.lse[(static_cast<long long>(b) * p.H + h) * p.S_q + q_row] = lse_from(m_used, l);
-        } else if (ok && p.n_split > 1) {
-            // ------------------------------------------------------------ epilogue: partial O, m, l
-            // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
-            // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
-            const long long row_lin = (static_cast<long long>(b) * p.H + h) * p.S_q + q_row;
-            const long long part = static_cast<long long>(split) * p.B * p.H * p.S_q + row_lin;
-            float *orow = p.part_o + part * p.D_v;
-            if (n_my > 0) tc_fence_after();
-            for (int cc = 0; cc < p.n_pv; cc += 16) {
-                uint32_t o[16];
-                if (n_my > 0) {
-                    tmem_ld16(o_addr + cc, o);
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k] = 0u;
-                }
-                if (!row_ok) continue;
-                if (cc + 16 <= p.D_v) {
-                    float4 *dst = reinterpret_cast<float4 *>(orow + cc);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
-                                             __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (cc + k < p.D_v) orow[cc + k] = __uint_as_float(o[k]);
-                }
+
+            if (ok && n_my > 0) {
+                ok = wait_bounded(smem_u32(&ctl.o_done[t]), o_par, ctl.abort_flag, p);
+                o_par ^= 1u;
+                ok = __all_sync(0xffffffffu, ok);
             }
-            if (row_ok) {
-                p.part_m[part] = n_my > 0 ? m_used : -INFINITY;
-                p.part_l[part] = n_my > 0 ? l : 0.0f;
+            const bool row_ok = q_row < p.S_q;
+            if (ok && p.n_split == 1) {
+                // ------------------------------------------------------------ epilogue: O = O_t / l
+                // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
+                if (n_my > 0) tc_fence_after();
+                const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
+                                (static_cast<long long>(U.b) * p.o_sb + static_cast<long long>(U.h) * p.o_sh +
+                                 static_cast<long long>(q_row) * p.o_ss) * 2;
+                for (int cc = 0; cc < p.n_pv; cc += 16) {
+                    uint32_t o[16];
+                    if (n_my > 0) {
+                        tmem_ld16(o_addr + cc, o);
+                        tmem_wait_ld();
+                    } else {
+                        #pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = 0u;
+                    }
+                    if (!row_ok) continue;
+                    uint32_t w[8];
+                    #pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+                    if (cc + 16 <= p.D_v) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
+                        #pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+                    }
+                }
+                if (p.lse && row_ok)
+                    p.lse[(static_cast<long long>(U.b) * p.H + U.h) * p.S_q + q_row] = lse_from(m_used, l);
+            } else if (ok && p.n_split > 1) {
+                // ------------------------------------------------------------ epilogue: partial O, m, l
+                // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
+                // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
+                const long long row_lin = (static_cast<long long>(U.b) * p.H + U.h) * p.S_q + q_row;
+                const long long part = static_cast<long long>(u % p.n_split) * p.B * p.H * p.S_q + row_lin;
+                float *orow = p.part_o + part * p.D_v;
+                if (n_my > 0) tc_fence_after();
+                for (int cc = 0; cc < p.n_pv; cc += 16) {
+                    uint32_t o[16];
+                    if (n_my > 0) {
+                        tmem_ld16(o_addr + cc, o);
+                        tmem_wait_ld();
+                    } else {
+                        #pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = 0u;
+                    }
+                    if (!row_ok) continue;
+                    if (cc + 16 <= p.D_v) {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + cc);
+                        #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                 __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                    } else {
+                        #pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) orow[cc + k] = __uint_as_float(o[k]);
+                    }
+                }
+                if (row_ok) {
+                    p.part_m[part] = n_my > 0 ? m_used : -INFINITY;
+                    p.part_l[part] = n_my > 0 ? l : 0.0f;
+                }
             }
         }
     }
@@ -522,6 +608,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (threadIdx.x == 0) sched_release(p);
 }
 
 }  // namespace vt
