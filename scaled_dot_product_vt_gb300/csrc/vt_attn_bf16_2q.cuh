@@ -12,7 +12,8 @@
 //   warp 0       TMA producer: per unit the Q tiles that have work (once the previous unit's last
 //                Q K^T has read Q), then K_0, V_0, K_1, V_1, ... through a ring of equal
 //                shared-memory slots (mbarrier full/empty per slot) that runs on across units.
-//   warp 1       TMEM owner and MMA issuer (one thread).  Per key tile j the tensor core runs
+//   warp 1       TMEM owner and MMA issuer (the whole warp runs the issuing code with warp-uniform
+//                values; one elected lane issues).  Per key tile j the tensor core runs
 //                  O_0 += P_0,j V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1,j V_j,  S_1 = Q_1 K_{j+1}^T
 //                so while softmax warpgroup t works on S_t, the tensor core works for the other
 //                tile.  Every operand descriptor is computed once; the K-steps are unrolled
@@ -290,7 +291,9 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this code with warp-uniform values and waits on every barrier; one lane
+        // chosen by elect.sync issues each MMA and commit.
+        {
             const uint32_t idesc_qk = instr_desc(1, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(1, kBM, p.n_pv, 1);
             // Descriptors as (low, high) words: offsets only move the low word (start address >> 4).
@@ -312,8 +315,12 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 
             // K/V slots are filled by TMA: the mbarrier's completed transaction count already makes
             // the bytes visible to the tensor core, so no tcgen05 fence is needed after this wait.
+            // Every lane waits, so whichever lane elect.sync picks has itself observed the phase.
+            auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl.abort_flag, p)) != 0;
+            };
             auto wait_full = [&](int s) -> bool {
-                const bool r = wait_bounded(smem_u32(&ctl.full[s]), (full_phase >> s) & 1u, ctl.abort_flag, p);
+                const bool r = wait1(smem_u32(&ctl.full[s]), (full_phase >> s) & 1u);
                 full_phase ^= 1u << s;
                 return r;
             };
@@ -321,20 +328,23 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < KQ; ++kk) {
                     const uint32_t off = (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2;
-                    mma_ss_w(d, q_lo + off, q_hi, k_lo + off, k_hi, idesc_qk, kk > 0);
+                    mma_ss_elect(d, q_lo + off, q_hi, k_lo + off, k_hi, idesc_qk, kk > 0);
                 }
             };
             auto pv = [&](uint32_t d, uint32_t a, uint32_t v_lo, uint32_t acc0) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts_w(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u);
+                    mma_ts_elect(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u);
             };
 
-            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook
+            if (p.flags & 1u) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
             int ks = 0;  // slot of the next K tile (the ring runs on across units)
             for (int n = 0; ok; ++n) {
-                int u;
-                if (!(ok = next_unit(ctl, n, &u, p)) || u < 0) break;
+                int u = -1;
+                if (lane == 0) ok = next_unit(ctl, n, &u, p);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (!ok || u < 0) break;
                 const Unit U = decode_unit(p, u);
                 const int n_kv = U.n_kv;
                 if (n_kv == 0) continue;
@@ -342,21 +352,21 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 // query tile t takes part in key tile j when as_t <= j < es_t
                 auto act0 = [&](int j) { return j >= as0 && j < es0; };
                 auto act1 = [&](int j) { return j >= as1 && j < es1; };
-                if (!(ok = wait_bounded(smem_u32(&ctl.q_full), q_par, ctl.abort_flag, p))) break;
+                if (!(ok = wait1(smem_u32(&ctl.q_full), q_par))) break;
                 q_par ^= 1u;
                 if (!(ok = wait_full(ks))) break;
                 {
                     const uint32_t k_lo = k_lo0 + ks * slot_step;
                     if (act0(0)) {
                         qk(s_col0, q_lo0, k_lo);
-                        mma_commit(smem_u32(&ctl.s_full[0]));
+                        mma_commit_elect(smem_u32(&ctl.s_full[0]));
                     }
                     if (act1(0)) {
                         qk(s_col1, q_lo1, k_lo);
-                        mma_commit(smem_u32(&ctl.s_full[1]));
+                        mma_commit_elect(smem_u32(&ctl.s_full[1]));
                     }
-                    if (n_kv == 1) mma_commit(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
-                    mma_commit(smem_u32(&ctl.empty[ks]));
+                    if (n_kv == 1) mma_commit_elect(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
+                    mma_commit_elect(smem_u32(&ctl.empty[ks]));
                     any_mma = true;
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
@@ -367,7 +377,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     const uint32_t v_lo = v_lo0 + vs * slot_step;
                     const uint32_t kn_lo = k_lo0 + kn * slot_step;
                     if (act0(j)) {
-                        if (!(ok = wait_bounded(smem_u32(&ctl.p_full[0]), p_par0, ctl.abort_flag, p))) break;
+                        if (!(ok = wait1(smem_u32(&ctl.p_full[0]), p_par0))) break;
                         p_par0 ^= 1u;
                         tc_fence_after();
                         pv(o_col0, s_col0, v_lo, j > as0);
@@ -375,31 +385,32 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     if (more && !(ok = wait_full(kn))) break;
                     if (act0(j + 1)) {
                         qk(s_col0, q_lo0, kn_lo);
-                        mma_commit(smem_u32(&ctl.s_full[0]));
+                        mma_commit_elect(smem_u32(&ctl.s_full[0]));
                     } else if (act0(j)) {
-                        mma_commit(smem_u32(&ctl.o_done[0]));
+                        mma_commit_elect(smem_u32(&ctl.o_done[0]));
                     }
                     if (act1(j)) {
-                        if (!(ok = wait_bounded(smem_u32(&ctl.p_full[1]), p_par1, ctl.abort_flag, p))) break;
+                        if (!(ok = wait1(smem_u32(&ctl.p_full[1]), p_par1))) break;
                         p_par1 ^= 1u;
                         tc_fence_after();
                         pv(o_col1, s_col1, v_lo, j > as1);
                     }
-                    mma_commit(smem_u32(&ctl.empty[vs]));
+                    mma_commit_elect(smem_u32(&ctl.empty[vs]));
                     if (act1(j + 1)) {
                         qk(s_col1, q_lo1, kn_lo);
-                        mma_commit(smem_u32(&ctl.s_full[1]));
+                        mma_commit_elect(smem_u32(&ctl.s_full[1]));
                     } else if (act1(j)) {
-                        mma_commit(smem_u32(&ctl.o_done[1]));
+                        mma_commit_elect(smem_u32(&ctl.o_done[1]));
                     }
-                    if (j + 2 == n_kv) mma_commit(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
-                    if (more) mma_commit(smem_u32(&ctl.empty[kn]));
+                    if (j + 2 == n_kv) mma_commit_elect(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
+                    if (more) mma_commit_elect(smem_u32(&ctl.empty[kn]));
                     ks = kn;
                 }
             }
             if (!ok && any_mma) {
-                mma_commit(smem_u32(&ctl.drain));
-                wait_drain(smem_u32(&ctl.drain), 0, p);
+                mma_commit_elect(smem_u32(&ctl.drain));
+                if (lane == 0) wait_drain(smem_u32(&ctl.drain), 0, p);
+                __syncwarp();
             }
         }
     }
