@@ -3,8 +3,9 @@
 // One CTA computes one work item: a 128-row query block of one (b, h) slice.  Warp roles:
 //   warp 0      TMA producer: the Q block once, then K and V tiles of BN keys through a
 //               `stages`-deep ring of shared-memory slots (mbarrier full/empty pairs).
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a TMEM score
-//               buffer (two buffers, alternating), then O += P_j V_j with P_j read from TMEM.
+//   warp 1      TMEM owner and MMA issuer (the whole warp; one elected lane issues): S_j = Q K_j^T
+//               into a TMEM score buffer (two buffers, alternating), then O += P_j V_j with P_j
+//               read from TMEM.
 //   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
 //               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
 //               over S_j, O rescale when the reference max moves, and the epilogue.
@@ -173,9 +174,10 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // Descriptors are built once as (low, high) words and the K-steps are unrolled (KQ):
-        // computing a descriptor per instruction would make this thread the bottleneck.
-        if (lane == 0 && n_kv > 0) {
+        // Descriptors are built once as (low, high) words and the K-steps are unrolled (KQ).  The
+        // whole warp runs this code with warp-uniform values and waits on every barrier; one lane
+        // chosen by elect.sync issues each MMA and commit.
+        if (n_kv > 0) {
             static_assert(DT == kF32, "this kernel serves fp32 I/O; bf16 uses the two-tile kernel");
             const uint32_t idesc_qk = instr_desc(C::kFmt, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(C::kFmt, kBM, p.n_pv, 0);
@@ -188,19 +190,23 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             const uint32_t stage_step = (k_bytes + v_bytes) >> 4;
             const uint32_t v_chunk = static_cast<uint32_t>(p.n_pv) * 8;  // one V^T key chunk, descriptor units
             bool ok = true, any_mma = false;
-            if (p.flags & 1u) ok = wait_bounded(smem_u32(&ctl.stall), 0, ctl.abort_flag, p);  // test hook: never signalled
-            if (ok) ok = wait_bounded(smem_u32(&ctl.q_full), 0, ctl.abort_flag, p);
+            // Every lane waits, so whichever lane elect.sync picks has itself observed the phase.
+            auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl.abort_flag, p)) != 0;
+            };
+            if (p.flags & 1u) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook: never signalled
+            if (ok) ok = wait1(smem_u32(&ctl.q_full), 0);
 
             auto issue_qk = [&](int j) -> bool {
                 const int st = j % p.stages;
-                if (!wait_bounded(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1, ctl.abort_flag, p)) return false;
+                if (!wait1(smem_u32(&ctl.full_k[st]), (j / p.stages) & 1)) return false;
                 const uint32_t d = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
                 const uint32_t k_lo = k_lo0 + st * stage_step;
 #pragma unroll
                 for (int kk = 0; kk < KQ; ++kk)
-                    mma_ss_tf32_w(d, q_lo + (kk >> 2) * (kBM * 8) + (kk & 3) * 2, q_hi,
+                    mma_ss_tf32_elect(d, q_lo + (kk >> 2) * (kBM * 8) + (kk & 3) * 2, q_hi,
                                   k_lo + (kk >> 2) * (BN * 8) + (kk & 3) * 2, k_hi, idesc_qk, kk > 0);
-                mma_commit(smem_u32(&ctl.s_full[j & 1]));
+                mma_commit_elect(smem_u32(&ctl.s_full[j & 1]));
                 any_mma = true;
                 return true;
             };
@@ -209,22 +215,23 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             for (int j = 0; ok && j < n_kv; ++j) {
                 if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
                 const int st = j % p.stages;
-                if (!wait_bounded(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1, ctl.abort_flag, p)) { ok = false; break; }
-                if (!wait_bounded(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1, ctl.abort_flag, p)) { ok = false; break; }
+                if (!wait1(smem_u32(&ctl.p_full[j & 1]), (j >> 1) & 1)) { ok = false; break; }
+                if (!wait1(smem_u32(&ctl.full_v[st]), (j / p.stages) & 1)) { ok = false; break; }
                 tc_fence_after();  // P was written to TMEM and V^T to shared memory by other warps
                 const uint32_t a_base = tmem + ((j & 1) ? C::kColS1 : C::kColS0);
                 const uint32_t v_lo = v_lo0 + st * stage_step;
                 // V^T K-major: K-step = 8 keys = 32 bytes inside a 128-byte key chunk
 #pragma unroll
                 for (int kk = 0; kk < BN / C::kKStep; ++kk)
-                    mma_ts_tf32_w(tmem + C::kColO, a_base + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi,
+                    mma_ts_tf32_elect(tmem + C::kColO, a_base + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi,
                                   idesc_pv, (j > 0 || kk > 0));
-                mma_commit(smem_u32(&ctl.empty[st]));
-                mma_commit(smem_u32(&ctl.o_done));
+                mma_commit_elect(smem_u32(&ctl.empty[st]));
+                mma_commit_elect(smem_u32(&ctl.o_done));
             }
             if (!ok && any_mma) {
-                mma_commit(smem_u32(&ctl.drain));
-                wait_drain(smem_u32(&ctl.drain), 0, p);
+                mma_commit_elect(smem_u32(&ctl.drain));
+                if (lane == 0) wait_drain(smem_u32(&ctl.drain), 0, p);
+                __syncwarp();
             }
         }
     } else if (DT == kF32 && warp >= 6) {
