@@ -93,6 +93,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.first = threading.Event()
 
     def start(self):
         try:
@@ -108,6 +109,14 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self.first.set()
+        self.first.set()
+
+    def wait_first(self, timeout: float = 15.0):
+        """Block until nvidia-smi has printed its first sample: its start-up (NVML initialisation)
+        can hold driver locks for seconds, which must not fall inside a timed region."""
+        if self.proc is not None:
+            self.first.wait(timeout)
 
     def stop(self):
         if self.proc is None:
@@ -321,6 +330,7 @@ def main() -> int:
     # ---- kernel-only timed region: inputs resident in HBM
     clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
     clocks.start()
+    clocks.wait_first()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
