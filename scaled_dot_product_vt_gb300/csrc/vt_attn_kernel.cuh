@@ -9,7 +9,7 @@
 //   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
 //               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
 //               over S_j, O rescale when the reference max moves, and the epilogue.
-//   warps 6-9   fp32 I/O only: V loader.  The TF32 MMA takes its B operand K-major only (an
+//   warps 6-13  fp32 I/O only: V loaders, two groups of four warps taking alternate key tiles.  The TF32 MMA takes its B operand K-major only (an
 //               N-major tf32 B reads as zeros), so V tiles are read with coalesced 16-byte
 //               loads and written transposed (keys contiguous) into the 128-byte-swizzled
 //               K-major layout; for bf16, V goes by TMA as it is (N-major B).
@@ -38,8 +38,11 @@ struct Cfg {
     static constexpr uint32_t kFmt = DT == kBF16 ? 1u : 2u;    // bf16 / tf32
     static constexpr uint32_t kTmemCols = DT == kBF16 ? 512u : 256u;
     static constexpr uint32_t kColS0 = 0, kColS1 = kBN, kColO = 2 * kBN;
-    static constexpr int kThreads = DT == kBF16 ? 192 : 320;
-    static constexpr int kVLoaders = DT == kBF16 ? 0 : 128;
+    // fp32: two V-loader groups of 128 threads take alternate key tiles, so two tiles' global
+    // reads are in flight at once (one group alone was bound by one read round trip per tile).
+    static constexpr int kVLoaderGroups = DT == kBF16 ? 0 : 2;
+    static constexpr int kVLoaders = DT == kBF16 ? 0 : 128;  // threads per group
+    static constexpr int kThreads = 192 + kVLoaderGroups * kVLoaders;
     // float4 loads per loader thread and V tile, at most (BN keys x 128 columns / 4 / loaders)
     static constexpr int kVLoadsPerThread = DT == kBF16 ? 1 : (64 * 128 / 4) / 128;
 };
@@ -236,12 +239,13 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
     } else if (DT == kF32 && warp >= 6) {
         // ------------------------------------------------------------ fp32 V loader (transposing)
-        const int lt = threadIdx.x - 192;
+        const int group = (threadIdx.x - 192) / C::kVLoaders;  // takes key tiles j = group (mod groups)
+        const int lt = (threadIdx.x - 192) % C::kVLoaders;
         const int nd4 = p.n_pv / 4;  // 4-column groups, including the zero padding up to n_pv
         const float *vbh = static_cast<const float *>(p.V) + static_cast<long long>(b) * p.v_sb +
                            static_cast<long long>(hk) * p.v_sh;
         uint8_t *smem_gen = smem_raw + (base - raw);
-        for (int j = 0; j < n_kv; ++j) {
+        for (int j = group; j < n_kv; j += C::kVLoaderGroups) {
             const int st = j % p.stages;
             const int use = j / p.stages;
             if (use > 0) {
@@ -251,13 +255,16 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             }
             uint8_t *dst = smem_gen + (sV(st) - base);
             // All of this thread's loads of the tile are issued before any store, so the tile
-            // costs one memory round trip rather than one per load.
+            // costs one memory round trip rather than one per load.  Item idx is (key, 4-column
+            // group) with the key fastest: a warp covers 32 consecutive keys of one group, so its
+            // transposed stores land on 32 different banks (the 128-byte swizzle spreads the 32
+            // keys of a row over all chunks), where columns-fastest items collided 10-fold.
             float4 val[C::kVLoadsPerThread];
 #pragma unroll
             for (int u = 0; u < C::kVLoadsPerThread; ++u) {
                 const int idx = lt + u * C::kVLoaders;
-                const int key = idx / nd4;
-                const int d0 = (idx - key * nd4) * 4;
+                const int key = idx % BN;
+                const int d0 = (idx / BN) * 4;
                 const int kg = (j_first + j) * BN + key;
                 val[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (idx < BN * nd4 && kg < p.S_k && d0 < p.D_v) {
@@ -275,8 +282,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             for (int u = 0; u < C::kVLoadsPerThread; ++u) {
                 const int idx = lt + u * C::kVLoaders;
                 if (idx >= BN * nd4) break;
-                const int key = idx / nd4;
-                const int d0 = (idx - key * nd4) * 4;
+                const int key = idx % BN;
+                const int d0 = (idx / BN) * 4;
                 uint8_t *chunk = dst + (key >> 5) * p.n_pv * 128;
                 const int kb = (key & 31) * 4;
                 *reinterpret_cast<float *>(chunk + swizzle128(d0 + 0, kb)) = val[u].x;
