@@ -67,7 +67,7 @@ struct SharedCtl {
     uint64_t q_full;
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t o_done;
+    uint64_t o_done[2];  // P_j V_j done, for j even / odd
     uint64_t drain;
     uint64_t stall;
     uint32_t tmem_base;
@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             mbar_init(smem_u32(&ctl.s_full[i]), 1);
             mbar_init(smem_u32(&ctl.p_full[i]), 128);
         }
-        mbar_init(smem_u32(&ctl.o_done), 1);
+        mbar_init(smem_u32(&ctl.o_done[0]), 1);
+        mbar_init(smem_u32(&ctl.o_done[1]), 1);
         mbar_init(smem_u32(&ctl.drain), 1);
         mbar_init(smem_u32(&ctl.stall), 1);
         ctl.abort_flag = 0;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                     mma_ts_tf32_elect(tmem + C::kColO, a_base + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi,
                                   idesc_pv, (j > 0 || kk > 0));
                 mma_commit_elect(smem_u32(&ctl.empty[st]));
-                mma_commit_elect(smem_u32(&ctl.o_done));
+                mma_commit_elect(smem_u32(&ctl.o_done[j & 1]));
             }
             if (!ok && any_mma) {
                 mma_commit_elect(smem_u32(&ctl.drain));
@@ -378,31 +379,39 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 for (int cc = 0; cc < BN / 32; ++cc) tmem_st32(s_addr + cc * 32, pk + cc * 32);
             }
 
-            // O *= alpha for rows whose reference moved, once P_{j-1} V_{j-1} has landed.
-            if (j > 0) {
-                ok = wait_bounded(smem_u32(&ctl.o_done), (j - 1) & 1, ctl.abort_flag, p);
+            // O *= alpha for rows whose reference moved, once P_{j-1} V_{j-1} has landed.  That
+            // wait sits before the hand-over of P_j only when a row rescales; otherwise the phase
+            // is consumed after the hand-over, off the chain S_j -> P_j -> P_j V_j.  With one
+            // barrier per parity of j, o_done[(j-1) & 1] cannot complete again before P_{j+1} is
+            // handed over, so a late wait never sees an ambiguous phase.
+            const bool fix_o = j > 0 && __any_sync(0xffffffffu, resc);
+            if (fix_o) {
+                ok = wait_bounded(smem_u32(&ctl.o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ctl.abort_flag, p);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, resc)) {
-                    const uint32_t o_addr = tmem + lane_base + C::kColO;
-                    for (int cc = 0; cc < p.n_pv; cc += 16) {
-                        uint32_t o[16];
-                        tmem_ld16(o_addr + cc, o);
-                        tmem_wait_ld();
+                const uint32_t o_addr = tmem + lane_base + C::kColO;
+                for (int cc = 0; cc < p.n_pv; cc += 16) {
+                    uint32_t o[16];
+                    tmem_ld16(o_addr + cc, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st16(o_addr + cc, o);
-                    }
+                    for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tmem_st16(o_addr + cc, o);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&ctl.p_full[j & 1]));
+            if (j > 0 && !fix_o) {
+                ok = wait_bounded(smem_u32(&ctl.o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ctl.abort_flag, p);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
         }
 
         if (ok && n_kv > 0) {
-            ok = wait_bounded(smem_u32(&ctl.o_done), (n_kv - 1) & 1, ctl.abort_flag, p);
+            ok = wait_bounded(smem_u32(&ctl.o_done[(n_kv - 1) & 1]), ((n_kv - 1) >> 1) & 1, ctl.abort_flag, p);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
