@@ -134,8 +134,9 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3],
  *                    vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) bytes, not overlapping
  *                    Q, K, V or O.  Its contents are scratch: overwritten by every call, and two
  *                    calls that share a workspace must not overlap on the GPU.
- * bf16 I/O only for n_split > 1 (fp32 I/O returns VT_ERR_UNSUPPORTED).  Other arguments and
- * errors as for vt_attn_fwd_strided; a too small or NULL workspace is VT_ERR_INVALID_ARG.
+ * Both element types (the fp32 shares cut 64-key tiles, the bf16 shares 128-key tiles).  Other
+ * arguments and errors as for vt_attn_fwd_strided; a too small or NULL workspace is
+ * VT_ERR_INVALID_ARG.
  */
 vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3],
                               const void *K, const int64_t k_stride[3],
@@ -152,8 +153,8 @@ vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3],
 size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split);
 
 /* The number of shares this library would pick on the current device: the most that still fit
- * one wave of CTAs with at least four 128-key tiles each; 1 when splitting does not pay (or for
- * fp32 I/O).  Queries the current device's SM count. */
+ * one wave of CTAs with at least four key tiles each (128 keys for bf16, 64 for fp32); 1 when
+ * splitting does not pay.  Queries the current device's SM count. */
 int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype);
 
 /*
@@ -214,7 +215,7 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3],
  * (the continuation case 4 of the attention_fwd_triton3 row).  Must be 4-byte aligned and must not
  * overlap Q, K, V, O or the workspace.
  *
- * n_split, workspace and workspace_bytes are those of vt_attn_fwd_splitkv (n_split > 1: bf16 only);
+ * n_split, workspace and workspace_bytes are those of vt_attn_fwd_splitkv;
  * opts those of vt_attn_fwd_ex (may be NULL); mask may be NULL (VT_MASK_NONE).  Errors as for
  * vt_attn_fwd_splitkv, and VT_ERR_INVALID_ARG for H_kv < 1, H not a multiple of H_kv, an unknown mask
  * kind, offset < 0, window < 1 with a window kind, or a misplaced lse; VT_ERR_UNSUPPORTED for

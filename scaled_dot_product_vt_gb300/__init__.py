@@ -208,7 +208,7 @@ def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None
 
 def attn_fwd_splitkv(q, k, v, scale: float | None = None, causal: bool = False, n_split: int | None = None,
                      out=None, workspace=None, stream=None):
-    """Split-KV forward for CUDA tensors (bf16 for n_split > 1).  ``n_split=None`` uses the
+    """Split-KV forward for CUDA tensors (bf16 or fp32).  ``n_split=None`` uses the
     library's choice; ``workspace`` may be a preallocated uint8 CUDA tensor of at least
     ``vt_attn_splitkv_workspace_size`` bytes (allocated here otherwise)."""
     import torch
@@ -244,7 +244,7 @@ def attn_fwd_general(q, k, v, scale: float | None = None, mask: str = "none", of
     """General forward for CUDA tensors: q [B,H,S_q,D_qk], k [B,H_kv,S_k,D_qk], v [B,H_kv,S_k,D_v] with H a
     multiple of H_kv (grouped heads), ``mask`` one of ``MASKS`` with ``offset`` and ``window`` (see
     include/vt_attn.h).  Returns O, or (O, LSE) with ``return_lse`` (LSE: float32 [B,H,S_q], natural log).
-    ``n_split`` > 1 runs the split-KV form (bf16); its workspace is allocated here unless given."""
+    ``n_split`` > 1 runs the split-KV form; its workspace is allocated here unless given."""
     import torch
     B, H, S_q, D_qk = q.shape
     H_kv, S_k, D_v = k.shape[1], k.shape[2], v.shape[3]

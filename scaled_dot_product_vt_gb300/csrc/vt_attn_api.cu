@@ -182,6 +182,29 @@ void band_of(const Problem &P, long long *lo, long long *hi, int *reverse) {
     }
 }
 
+// Combine the n_split partial results of every row into O (and the LSE if asked for).
+template <int ELT>
+vt_status merge(const AttnParams &p, const Problem &P, cudaStream_t stream) {
+    MergeParams mp{};
+    mp.part_o = p.part_o;
+    mp.part_m = p.part_m;
+    mp.part_l = p.part_l;
+    mp.O = P.O;
+    mp.lse = P.lse;
+    mp.rows = P.B * P.H * P.S_q;
+    mp.H = static_cast<int>(P.H);
+    mp.S_q = static_cast<int>(P.S_q);
+    mp.D_v = static_cast<int>(P.D_v);
+    mp.n_split = p.n_split;
+    mp.o_sb = P.os[0];
+    mp.o_sh = P.os[1];
+    mp.o_ss = P.os[2];
+    const long long blocks = (mp.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock;
+    if (blocks > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+    attn_merge_kernel<ELT><<<static_cast<unsigned>(blocks), 32 * kMergeRowsPerBlock, 0, stream>>>(mp);
+    return cudaGetLastError() == cudaSuccess ? VT_OK : VT_ERR_CUDA;
+}
+
 template <int DT>
 vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *workspace, cudaStream_t stream) {
     using C = Cfg<DT>;
@@ -273,26 +296,7 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<grid, q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
-        if (n_split > 1) {
-            MergeParams mp{};
-            mp.part_o = p.part_o;
-            mp.part_m = p.part_m;
-            mp.part_l = p.part_l;
-            mp.O = O;
-            mp.lse = P.lse;
-            mp.rows = B * H * S_q;
-            mp.H = static_cast<int>(H);
-            mp.S_q = static_cast<int>(S_q);
-            mp.D_v = static_cast<int>(D_v);
-            mp.n_split = n_split;
-            mp.o_sb = os[0];
-            mp.o_sh = os[1];
-            mp.o_ss = os[2];
-            const long long blocks = (mp.rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock;
-            if (blocks > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
-            attn_merge_kernel<2><<<static_cast<unsigned>(blocks), 32 * kMergeRowsPerBlock, 0, stream>>>(mp);
-            if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
-        }
+        if (n_split > 1) return merge<2>(p, P, stream);
         return VT_OK;
     } else {
         // one 128-row query tile per CTA (fp32 I/O on the TF32 path)
@@ -311,12 +315,12 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
                         : chunks == 2 ? attn_fwd_kernel<DT, 8>
                                       : chunks == 3 ? attn_fwd_kernel<DT, 12> : attn_fwd_kernel<DT, 16>;
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
-        p.n_split = 1;  // split-KV is served by the bf16 kernel only
-        const long long items = static_cast<long long>(p.n_qblocks) * B * H;
+        const long long items = static_cast<long long>(p.n_qblocks) * B * H * n_split;
         if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         p.n_units = static_cast<int>(items);
         kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
+        if (n_split > 1) return merge<4>(p, P, stream);
         return VT_OK;
     }
 }
@@ -425,12 +429,11 @@ vt_status check_args(const Problem &P, bool *empty) {
 // Checks of a split-KV workspace (n_split > 1): present, large enough, 256-byte aligned and clear of
 // every tensor of the call.
 vt_status check_workspace(const Problem &P, int n_split, const void *workspace, size_t workspace_bytes) {
-    if (P.dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < vt::split_layout(P.B, P.H, P.S_q, P.D_v, n_split).bytes)
         return VT_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 256) return VT_ERR_MISALIGNED;
     const vt::Span w{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + workspace_bytes};
-    const int elt = 2;
+    const int elt = P.dtype == VT_BF16 ? 2 : 4;
     if (vt::overlap(w, vt::span_of(P.Q, P.qs, P.B, P.H, P.S_q, P.D_qk, elt)) ||
         vt::overlap(w, vt::span_of(P.K, P.ks, P.B, P.H_kv, P.S_k, P.D_qk, elt)) ||
         vt::overlap(w, vt::span_of(P.V, P.vs, P.B, P.H_kv, P.S_k, P.D_v, elt)) ||
@@ -521,14 +524,17 @@ size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
 
 int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype) {
     (void)causal;
-    if (dtype != VT_BF16 || B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return 1;
+    if ((dtype != VT_BF16 && dtype != VT_F32) || B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
     // Shares only pay when every CTA still fits in one wave, and each share keeps >= 4 key tiles.
-    const long long items = B * H * ((S_q + vt::q2::kRows - 1) / vt::q2::kRows);
-    const long long tiles = (S_k + vt::q2::kBN - 1) / vt::q2::kBN;
+    // work items and key tiles of the kernel that serves the dtype
+    const long long rows = dtype == VT_BF16 ? vt::q2::kRows : vt::kBM;
+    const long long bn = dtype == VT_BF16 ? vt::q2::kBN : vt::Cfg<vt::kF32>::kBN;
+    const long long items = B * H * ((S_q + rows - 1) / rows);
+    const long long tiles = (S_k + bn - 1) / bn;
     long long n = items >= sms ? 1 : sms / items;
     if (n > tiles / 4) n = tiles / 4;
     if (n > vt::kMaxSplit) n = vt::kMaxSplit;
@@ -570,7 +576,6 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], 
     if (empty) return VT_OK;
     void *scratch = nullptr;
     if (n_split > 1) {
-        if (dtype != VT_BF16) return VT_ERR_UNSUPPORTED;
         // The shares' partial results must fit the fixed array; nothing is allocated instead.
         if (vt::split_layout(B, H, S_q, D_v, n_split).bytes > vt::kNoAllocScratchBytes) return VT_ERR_UNSUPPORTED;
         int dev = 0;

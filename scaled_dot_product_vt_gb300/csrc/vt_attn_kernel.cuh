@@ -87,19 +87,27 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: all heads' heaviest query blocks first when work grows with the block index.
+    // Work item: all heads' heaviest query blocks first when work grows with the block index;
+    // with split-KV, the n_split shares of one item are adjacent in the launch order.
+    const int split = blockIdx.x % p.n_split;
+    const int item = blockIdx.x / p.n_split;
     const int bh_count = p.B * p.H;
-    const int slot = blockIdx.x / bh_count;
-    const int bh = blockIdx.x - slot * bh_count;
+    const int slot = item / bh_count;
+    const int bh = item - slot * bh_count;
     const int qb = p.reverse_q ? (p.n_qblocks - 1 - slot) : slot;
     const int h = bh % p.H;
     const int b = bh / p.H;
     const int hk = h / p.kv_group;  // key/value head
     const int q_row0 = qb * kBM;
     // key tiles [j_first, j_first + n_kv) that some row of the block may see (none: n_kv = 0)
+    // and this CTA's contiguous share of them
     int j_first, j_end;
     band_tiles(p, q_row0, min(q_row0 + kBM, p.S_q) - 1, BN, &j_first, &j_end);
-    const int n_kv = j_end - j_first;
+    const int n_all = j_end - j_first;
+    const int per = (n_all + p.n_split - 1) / p.n_split;
+    const int share_lo = min(split * per, n_all);
+    j_first += share_lo;
+    const int n_kv = min(n_all, share_lo + per) - share_lo;
 
     // Shared-memory carve-up (1024-byte aligned for the 128-byte swizzle).
     const uint32_t raw = smem_u32(smem_raw);
@@ -416,8 +424,44 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
         if (ok) {
             // ------------------------------------------------------------ epilogue
-            // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
+            // A row with no allowed key (l = 0, or no key tile at all) is written as 0; with
+            // split-KV the share writes its unnormalised O with its reference max m (log2 units)
+            // and sum l instead (the empty share: O = 0, m = -inf, l = 0), and the merge kernel
+            // finishes the row.
             if (n_kv > 0) tc_fence_after();
+            if (p.n_split > 1) {
+                const uint32_t o_addr = tmem + lane_base + C::kColO;
+                const bool row_ok = q_row < p.S_q;
+                const long long row_lin = (static_cast<long long>(b) * p.H + h) * p.S_q + q_row;
+                const long long part = static_cast<long long>(split) * p.B * p.H * p.S_q + row_lin;
+                float *prow = p.part_o + part * p.D_v;
+                for (int cc = 0; cc < p.n_pv; cc += 16) {
+                    uint32_t o[16];
+                    if (n_kv > 0) {
+                        tmem_ld16(o_addr + cc, o);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = 0u;
+                    }
+                    if (!row_ok) continue;
+                    if (cc + 16 <= p.D_v) {
+                        float4 *dst = reinterpret_cast<float4 *>(prow + cc);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                 __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (cc + k < p.D_v) prow[cc + k] = __uint_as_float(o[k]);
+                    }
+                }
+                if (row_ok) {
+                    p.part_m[part] = n_kv > 0 ? m_used : -INFINITY;
+                    p.part_l[part] = n_kv > 0 ? l : 0.0f;
+                }
+            } else {
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
             const uint32_t o_addr = tmem + lane_base + C::kColO;
             const bool row_ok = q_row < p.S_q;
@@ -466,6 +510,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             }
             if (p.lse && row_ok)
                 p.lse[(static_cast<long long>(b) * p.H + h) * p.S_q + q_row] = lse_from(m_used, l);
+            }
         }
     }
 

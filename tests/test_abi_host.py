@@ -113,8 +113,8 @@ def split_call(n_split=2, dtype=vt.VT_BF16, ws=8 * A, ws_bytes=1 << 24, D_v=8):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(n_split=0), 1), (dict(n_split=-3), 1), (dict(n_split=65), 2),
-    (dict(dtype=vt.VT_F32), 2),                       # split-KV serves bf16 only
     (dict(ws=None), 1), (dict(ws_bytes=64), 1),       # missing or too small workspace
+    (dict(dtype=vt.VT_F32, ws_bytes=64), 1),          # fp32 partials need more workspace too
     (dict(ws=8 * A + 16), 3),                         # workspace not 256-byte aligned
     (dict(ws=A), 1),                                  # workspace overlaps Q
 ])
@@ -152,7 +152,6 @@ def general_call(H=4, H_kv=2, kind=0, offset=0, window=0, reserved=0, lse=None, 
     (dict(lse=A + 16), 1),                                          # lse overlaps Q
     (dict(n_split=0), 1), (dict(n_split=65), 2),
     (dict(n_split=2), 1),                                           # no workspace
-    (dict(n_split=2, ws=8 * A, ws_bytes=1 << 24, dtype=vt.VT_F32), 2),
     (dict(n_split=2, ws=8 * A, ws_bytes=1 << 24, lse=8 * A + 64), 1),  # lse inside the workspace
 ])
 def test_general_argument_errors(lib, kw, code):
@@ -169,4 +168,7 @@ def test_general_empty_problem_and_null_mask(lib):
     # a valid call with mask NULL reaches the launch, which reports the missing GPU
     assert general_call(mask=False) == 4
     assert general_call(kind=3, offset=2, window=5, lse=16 * A) == 4
+    # fp32 I/O with split-KV passes every argument check and reaches the launch
+    assert general_call(n_split=2, ws=8 * A, ws_bytes=1 << 24, dtype=vt.VT_F32) == 4
+    assert split_call(dtype=vt.VT_F32) == 4
     assert vt.vt_last_device_status(0) == 4

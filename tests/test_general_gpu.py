@@ -78,6 +78,8 @@ CASES = {
     "split_gqa_offset": ("bf16", 1, 8, 2, 200, 3000, 128, 128, "causal", 2800, 0, 5),
     "split_complement": ("bf16", 1, 2, 2, 300, 2000, 64, 64, "window_complement", 1700, 500, 3),
     "split_window_empty_shares": ("bf16", 1, 2, 1, 300, 4000, 64, 64, "window", 0, 100, 8),
+    "f32_split_window": ("f32", 1, 2, 2, 300, 2000, 64, 64, "window", 1700, 500, 3),
+    "f32_split_gqa_complement": ("f32", 1, 4, 1, 256, 1500, 32, 32, "window_complement", 1200, 300, 4),
 }
 
 

@@ -50,6 +50,27 @@ def test_splitkv_matches_oracle(case):
     assert np.abs(got - plain).max() <= 2e-2
 
 
+CASES_F32 = [
+    # B, H, S_q, S_k, D_qk, D_v, causal, n_split (fp32 I/O, TF32 path; 64-key tiles)
+    (2, 4, 1000, 1000, 72, 72, True, 2),    # the mid fp32 workload's shape
+    (1, 2, 200, 3000, 64, 48, False, 5),
+    (1, 1, 100, 130, 20, 20, False, 3),     # three key tiles, one per share
+    (1, 2, 130, 1000, 128, 128, True, 4),   # early rows have no key in the later shares
+    (1, 1, 64, 256, 32, 32, True, 8),       # more shares than key tiles: empty shares
+]
+
+
+@pytest.mark.parametrize("case", CASES_F32, ids=str)
+def test_splitkv_fp32_matches_oracle(case):
+    B, H, S_q, S_k, D_qk, D_v, causal, n_split = case
+    q, k, v = synth.make_qkv(B, H, S_q, S_k, D_qk, D_v, "f32", dist="uniform", seed=(hash(case) & 0xFFFF) + 5)
+    scale = float(np.float32(1.0 / math.sqrt(D_qk)))
+    Q, K, V = to_device(q), to_device(k), to_device(v)
+    got = to_host64(vt.attn_fwd_splitkv(Q, K, V, scale=scale, causal=causal, n_split=n_split))
+    assert vt.vt_last_device_status() == 0
+    check(got, oracle.attn_fwd(q, k, v, scale, causal), "f32", f"fp32 split-KV {case}")
+
+
 def test_splitkv_workspace_reuse_and_auto_choice():
     """One workspace serves calls with different share counts; the library's choice is used when none is given."""
     B, H, S_q, S_k, D = 1, 4, 128, 16384, 128
