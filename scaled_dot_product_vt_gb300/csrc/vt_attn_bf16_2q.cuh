@@ -1,5 +1,6 @@
-// Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per CTA sharing every
-// 128-key K/V tile, one softmax warpgroup per query tile, single-thread tcgen05 issue.
+// Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per work unit sharing every
+// 128-key K/V tile, one softmax warpgroup per query tile, tcgen05 issued by one warp (one lane
+// elected per instruction).
 //
 // Persistent: one CTA per SM takes work units in launch order from a global counter (the
 // producer warp draws them and passes them to the other roles through a small ring in shared
