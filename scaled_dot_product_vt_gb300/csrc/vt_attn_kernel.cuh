@@ -264,41 +264,51 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             }
             uint8_t *dst = smem_gen + (sV(st) - base);
             // All of this thread's loads of the tile are issued before any store, so the tile
-            // costs one memory round trip rather than one per load.  Item idx is (key, 4-column
-            // group) with the key fastest: a warp covers 32 consecutive keys of one group, so its
-            // transposed stores land on 32 different banks (the 128-byte swizzle spreads the 32
-            // keys of a row over all chunks), where columns-fastest items collided 10-fold.
-            float4 val[C::kVLoadsPerThread];
+            // costs one memory round trip rather than one per load.  An item is a block of 4 keys
+            // x 4 columns: four 16-byte row loads, a register transpose, and four 16-byte stores
+            // of 4 consecutive keys of one column (16 contiguous bytes of V^T, which the 128-byte
+            // swizzle keeps together).  Items run key-group fastest, so each 8-lane store phase
+            // covers 8 different 16-byte units of a row.
+            constexpr int kItems = C::kVLoadsPerThread / 4;  // 4x4 blocks per thread, at most
+            float4 blk[kItems][4];
+            const int n_items = (BN / 4) * nd4;
 #pragma unroll
-            for (int u = 0; u < C::kVLoadsPerThread; ++u) {
-                const int idx = lt + u * C::kVLoaders;
-                const int key = idx % BN;
-                const int d0 = (idx / BN) * 4;
-                const int kg = (j_first + j) * BN + key;
-                val[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (idx < BN * nd4 && kg < p.S_k && d0 < p.D_v) {
-                    const float *src = vbh + static_cast<long long>(kg) * p.v_ss + d0;
-                    if (d0 + 4 <= p.D_v) {
-                        val[u] = __ldg(reinterpret_cast<const float4 *>(src));
-                    } else {
-                        val[u].x = __ldg(src);
-                        if (d0 + 1 < p.D_v) val[u].y = __ldg(src + 1);
-                        if (d0 + 2 < p.D_v) val[u].z = __ldg(src + 2);
+            for (int u = 0; u < kItems; ++u) {
+                const int item = lt + u * C::kVLoaders;
+                const int kg = item % (BN / 4);
+                const int d0 = (item / (BN / 4)) * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int kglob = (j_first + j) * BN + kg * 4 + i;
+                    blk[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (item < n_items && kglob < p.S_k && d0 < p.D_v) {
+                        const float *src = vbh + static_cast<long long>(kglob) * p.v_ss + d0;
+                        if (d0 + 4 <= p.D_v) {
+                            blk[u][i] = __ldg(reinterpret_cast<const float4 *>(src));
+                        } else {
+                            blk[u][i].x = __ldg(src);
+                            if (d0 + 1 < p.D_v) blk[u][i].y = __ldg(src + 1);
+                            if (d0 + 2 < p.D_v) blk[u][i].z = __ldg(src + 2);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < C::kVLoadsPerThread; ++u) {
-                const int idx = lt + u * C::kVLoaders;
-                if (idx >= BN * nd4) break;
-                const int key = idx % BN;
-                const int d0 = (idx / BN) * 4;
-                uint8_t *chunk = dst + (key >> 5) * p.n_pv * 128;
-                const int kb = (key & 31) * 4;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 0, kb)) = val[u].x;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 1, kb)) = val[u].y;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 2, kb)) = val[u].z;
-                *reinterpret_cast<float *>(chunk + swizzle128(d0 + 3, kb)) = val[u].w;
+            for (int u = 0; u < kItems; ++u) {
+                const int item = lt + u * C::kVLoaders;
+                if (item >= n_items) break;
+                const int kg = item % (BN / 4);
+                const int d0 = (item / (BN / 4)) * 4;
+                uint8_t *chunk = dst + (kg >> 3) * p.n_pv * 128;  // 32 keys per 128-byte V^T row chunk
+                const uint32_t unit = static_cast<uint32_t>(kg & 7);
+                const float4 c0 = make_float4(blk[u][0].x, blk[u][1].x, blk[u][2].x, blk[u][3].x);
+                const float4 c1 = make_float4(blk[u][0].y, blk[u][1].y, blk[u][2].y, blk[u][3].y);
+                const float4 c2 = make_float4(blk[u][0].z, blk[u][1].z, blk[u][2].z, blk[u][3].z);
+                const float4 c3 = make_float4(blk[u][0].w, blk[u][1].w, blk[u][2].w, blk[u][3].w);
+                *reinterpret_cast<float4 *>(chunk + (d0 + 0) * 128 + ((unit ^ ((d0 + 0) & 7)) << 4)) = c0;
+                *reinterpret_cast<float4 *>(chunk + (d0 + 1) * 128 + ((unit ^ ((d0 + 1) & 7)) << 4)) = c1;
+                *reinterpret_cast<float4 *>(chunk + (d0 + 2) * 128 + ((unit ^ ((d0 + 2) & 7)) << 4)) = c2;
+                *reinterpret_cast<float4 *>(chunk + (d0 + 3) * 128 + ((unit ^ ((d0 + 3) & 7)) << 4)) = c3;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(smem_u32(&ctl.full_v[st]));
