@@ -9,7 +9,8 @@
 //   warps 2-5   softmax warpgroup, one query row per thread: S_j from TMEM, masks, running
 //               max with lazy rescaling, exp2 with the folded scale, P_j back into TMEM
 //               over S_j, O rescale when the reference max moves, and the epilogue.
-//   warps 6-13  fp32 I/O only: V loaders, two groups of four warps taking alternate key tiles.  The TF32 MMA takes its B operand K-major only (an
+//   warps 6-15  fp32 I/O only: V loaders, two groups of four warps taking alternate key tiles
+//               (warps 9 and 13 idle: no loader on the MMA warp's sub-partition).  The TF32 MMA takes its B operand K-major only (an
 //               N-major tf32 B reads as zeros), so V tiles are read with coalesced 16-byte
 //               loads and written transposed (keys contiguous) into the 128-byte-swizzled
 //               K-major layout; for bf16, V goes by TMA as it is (N-major B).
@@ -42,7 +43,9 @@ struct Cfg {
     // reads are in flight at once (one group alone was bound by one read round trip per tile).
     static constexpr int kVLoaderGroups = DT == kBF16 ? 0 : 2;
     static constexpr int kVLoaders = DT == kBF16 ? 0 : 128;  // threads per group
-    static constexpr int kThreads = 192 + kVLoaderGroups * kVLoaders;
+    // fp32: warps 6-15, of which 9 and 13 stay idle so that no loader shares sub-partition 1 with
+    // the MMA warp (16 warps cost no more registers per thread than 14)
+    static constexpr int kThreads = DT == kBF16 ? 192 : 512;
     // float4 loads per loader thread and V tile, at most (BN keys x 128 columns / 4 / loaders)
     static constexpr int kVLoadsPerThread = DT == kBF16 ? 1 : (64 * 128 / 4) / 128;
 };
@@ -248,8 +251,11 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         }
     } else if (DT == kF32 && warp >= 6) {
         // ------------------------------------------------------------ fp32 V loader (transposing)
-        const int group = (threadIdx.x - 192) / C::kVLoaders;  // takes key tiles j = group (mod groups)
-        const int lt = (threadIdx.x - 192) % C::kVLoaders;
+      if (warp != 9 && warp != 13) {  // warps 9 and 13 stay idle
+        const int wl = warp - 6;
+        const int li = wl - (wl > 3) - (wl > 7);               // loader warp 0..7
+        const int group = li >> 2;                             // takes key tiles j = group (mod groups)
+        const int lt = (li & 3) * 32 + lane;
         const int nd4 = p.n_pv / 4;  // 4-column groups, including the zero padding up to n_pv
         const float *vbh = static_cast<const float *>(p.V) + static_cast<long long>(b) * p.v_sb +
                            static_cast<long long>(hk) * p.v_sh;
@@ -313,6 +319,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(smem_u32(&ctl.full_v[st]));
         }
+      }
     } else {
         // ------------------------------------------------------------ softmax warpgroup
         const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
