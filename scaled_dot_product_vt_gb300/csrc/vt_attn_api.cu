@@ -62,6 +62,7 @@ bool env_check() {
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
+    long long l2_bytes = 0;
     unsigned *status = nullptr;
     unsigned *sched = nullptr;  // g_sched on this device
 };
@@ -83,6 +84,9 @@ bool device_info(int dev, DeviceInfo *out) {
     if (!d.ready) {
         void *status_ptr = nullptr, *sched_ptr = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return false;
+        d.l2_bytes = l2;
         if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return false;
         if (cudaGetSymbolAddress(&sched_ptr, g_sched) != cudaSuccess) return false;
         d.status = static_cast<unsigned *>(status_ptr);
@@ -276,9 +280,15 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         if (p.stages < 2) return VT_ERR_UNSUPPORTED;
         const int smem = 1024 + q_bytes + p.stages * slot_bytes;
         // Interleave the query blocks of about two waves' worth of heads, so the CTAs in flight
-        // share their heads' K and V in L2.
+        // share their heads' K and V in L2, but no more heads than three quarters of L2 holds K and
+        // V for: otherwise a head's blocks fall into different waves and its K/V is read again.
         const long long bh = B * H;
         long long grp = (2LL * sms + p.n_qblocks - 1) / p.n_qblocks;
+        // (consecutive query heads share one K/V head when H_kv < H)
+        const long long kv_head_bytes = S_k * (D_qk + D_v) * C::kElt;
+        const long long l2_heads =
+            info.l2_bytes > 0 ? (3 * info.l2_bytes / 4) / kv_head_bytes * (H / P.H_kv) : grp;
+        if (grp > l2_heads) grp = l2_heads;
         p.head_group = static_cast<int>(grp < 1 ? 1 : (grp > bh ? bh : grp));
         const long long units = static_cast<long long>(p.n_qblocks) * bh * n_split;
         if (units > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
