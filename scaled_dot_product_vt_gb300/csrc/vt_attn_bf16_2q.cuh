@@ -64,6 +64,14 @@ constexpr float kTau = 32.0f;
 __host__ __device__ constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t * 128); }
 __host__ __device__ constexpr uint32_t col_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
 
+// One work unit: a 256-row query block of one (b, h) and one share of its key tiles.
+struct Unit {
+    int u, split;             // launch-order index (-1: no more units) and split-KV share
+    int b, h, hk, r0;
+    int j0, n_kv;             // the share's first key tile and its number of key tiles
+    int as0, es0, as1, es1;   // key tiles [as_t, es_t) of the share that query tile t needs
+};
+
 struct Ctl {
     uint64_t full[kMaxSlots];
     uint64_t empty[kMaxSlots];
@@ -72,9 +80,9 @@ struct Ctl {
     uint64_t s_full[2];   // scores of tile t ready (and every earlier MMA done)
     uint64_t p_full[2];   // P of tile t written (128 arrivals)
     uint64_t o_done[2];   // last P V of tile t done
-    uint64_t unit_full[kUnitRing];   // unit index k written by the producer
-    uint64_t unit_empty[kUnitRing];  // unit index k read by every other role
-    int unit_id[kUnitRing];          // the unit, or -1 once the counter is exhausted
+    uint64_t unit_full[kUnitRing];   // ring entry k written by the producer
+    uint64_t unit_empty[kUnitRing];  // ring entry k read by every other role
+    Unit unit[kUnitRing];            // decoded units (u = -1 once the counter is exhausted)
     uint64_t drain;
     uint64_t stall;
     uint32_t tmem_base;
@@ -87,18 +95,14 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// One work unit: a 256-row query block of one (b, h) and one share of its key tiles.
-struct Unit {
-    int b, h, hk, r0;
-    int j0, n_kv;             // the share's first key tile and its number of key tiles
-    int as0, es0, as1, es1;   // key tiles [as_t, es_t) of the share that query tile t needs
-};
 
 // Units run over groups of `head_group` heads; inside a group, the heaviest query blocks first
 // when work grows with the block index; the shares of one block are adjacent.
 __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
     Unit U;
     const int split = u % p.n_split;
+    U.u = u;
+    U.split = split;
     const int item = u / p.n_split;
     const int BH = p.B * p.H;
     const int per_group = p.head_group * p.n_qblocks;
@@ -150,13 +154,30 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
     return U;
 }
 
-// The n-th unit this CTA works on, as the producer published it (-1: no more units); false on
-// abort.  Every reader calls it once per n, in order, and releases the ring entry.
-__device__ __forceinline__ bool next_unit(Ctl &ctl, int n, int *u, const AttnParams &p) {
+// The n-th unit this CTA works on, as the producer decoded and published it (u = -1: no more
+// units); false on abort.  Called by a whole warp: lane 0 waits for the ring entry and releases it,
+// every lane copies the unit (the producer decodes ahead, so readers spend no time on it).
+__device__ __forceinline__ bool next_unit(Ctl &ctl, int n, Unit *out, const AttnParams &p, int lane) {
     const int k = n % kUnitRing;
-    if (!wait_bounded(smem_u32(&ctl.unit_full[k]), (n / kUnitRing) & 1, ctl.abort_flag, p)) return false;
-    *u = *reinterpret_cast<volatile int *>(&ctl.unit_id[k]);
-    mbar_arrive(smem_u32(&ctl.unit_empty[k]));
+    bool ok = true;
+    if (lane == 0) ok = wait_bounded(smem_u32(&ctl.unit_full[k]), (n / kUnitRing) & 1, ctl.abort_flag, p);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    __syncwarp();
+    const volatile Unit *src = &ctl.unit[k];
+    out->u = src->u;
+    out->split = src->split;
+    out->b = src->b;
+    out->h = src->h;
+    out->hk = src->hk;
+    out->r0 = src->r0;
+    out->j0 = src->j0;
+    out->n_kv = src->n_kv;
+    out->as0 = src->as0;
+    out->es0 = src->es0;
+    out->as1 = src->as1;
+    out->es1 = src->es1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctl.unit_empty[k]));
     return true;
 }
 
@@ -241,10 +262,28 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
                 const unsigned drawn = atomicAdd(&p.sched[0], 1u);
                 const int u = drawn < static_cast<unsigned>(p.n_units) ? static_cast<int>(drawn) : -1;
-                *reinterpret_cast<volatile int *>(&ctl.unit_id[k]) = u;
+                Unit U;
+                if (u >= 0) {
+                    U = decode_unit(p, u);
+                } else {
+                    U.u = -1;
+                    U.split = U.b = U.h = U.hk = U.r0 = U.j0 = U.n_kv = U.as0 = U.es0 = U.as1 = U.es1 = 0;
+                }
+                volatile Unit *dst_u = &ctl.unit[k];
+                dst_u->u = U.u;
+                dst_u->split = U.split;
+                dst_u->b = U.b;
+                dst_u->h = U.h;
+                dst_u->hk = U.hk;
+                dst_u->r0 = U.r0;
+                dst_u->j0 = U.j0;
+                dst_u->n_kv = U.n_kv;
+                dst_u->as0 = U.as0;
+                dst_u->es0 = U.es0;
+                dst_u->as1 = U.as1;
+                dst_u->es1 = U.es1;
                 mbar_arrive(smem_u32(&ctl.unit_full[k]));
                 if (u < 0) break;
-                const Unit U = decode_unit(p, u);
                 if (U.n_kv == 0) continue;
                 if (q_loads > 0) {  // the previous unit's last Q K^T has read Q
                     ok = wait_bounded(smem_u32(&ctl.q_empty), (q_loads - 1) & 1, ctl.abort_flag, p);
@@ -341,12 +380,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             if (p.flags & 1u) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
             int ks = 0;  // slot of the next K tile (the ring runs on across units)
             for (int n = 0; ok; ++n) {
-                int u = -1;
-                if (lane == 0) ok = next_unit(ctl, n, &u, p);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                u = __shfl_sync(0xffffffffu, u, 0);
-                if (!ok || u < 0) break;
-                const Unit U = decode_unit(p, u);
+                Unit U;
+                if (!(ok = next_unit(ctl, n, &U, p, lane)) || U.u < 0) break;
                 const int n_kv = U.n_kv;
                 if (n_kv == 0) continue;
                 const int as0 = U.as0, es0 = U.es0, as1 = U.as1, es1 = U.es1;
@@ -432,12 +467,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         bool ok = true;
 
         for (int n = 0; ok; ++n) {
-            int u = -1;
-            if (lane == 0) ok = next_unit(ctl, n, &u, p);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            u = __shfl_sync(0xffffffffu, u, 0);
-            if (!ok || u < 0) break;
-            const Unit U = decode_unit(p, u);
+            Unit U;
+            if (!(ok = next_unit(ctl, n, &U, p, lane)) || U.u < 0) break;
             const int tile_row0 = U.r0 + t * kBM;
             const int q_row = tile_row0 + row;
             const int as_my = t ? U.as1 : U.as0;
@@ -580,7 +611,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
                 // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
                 const long long row_lin = (static_cast<long long>(U.b) * p.H + U.h) * p.S_q + q_row;
-                const long long part = static_cast<long long>(u % p.n_split) * p.B * p.H * p.S_q + row_lin;
+                const long long part = static_cast<long long>(U.split) * p.B * p.H * p.S_q + row_lin;
                 float *orow = p.part_o + part * p.D_v;
                 if (n_my > 0) tc_fence_after();
                 for (int cc = 0; cc < p.n_pv; cc += 16) {
