@@ -437,7 +437,7 @@ def main() -> int:
             "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                     "ms_per_step": e2e_ms / args.steps, "pipelined": True},
-            "gpu_launches": args.steps,  # kernel-only timed region: one launch per step
+            "gpu_launches": world * args.steps,  # kernel-only timed region: one launch per step and rank
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
         }
         print(json.dumps(line), flush=True)
