@@ -40,7 +40,9 @@
  *   VT_ERR_INVALID_ARG   a NULL pointer, a negative extent, S_k, D_qk or D_v equal to 0,
  *                        an unknown dtype, a non-finite scale, O overlapping Q/K/V,
  *                        or a non-positive stride;
- *   VT_ERR_UNSUPPORTED   D_qk or D_v above 128, or an extent beyond 2^31 - 1;
+ *   VT_ERR_UNSUPPORTED   D_qk or D_v above 128, S_q or S_k above 2^30, B or H above
+ *                        2^31 - 1, or more than 2^31 - 1 work units (query blocks x heads x
+ *                        batches x split-KV shares);
  *   VT_ERR_MISALIGNED    a pointer not 16-byte aligned, or a (b, h, s) stride whose
  *                        byte size is not a multiple of 16 (the TMA engine's rule);
  *   VT_ERR_CUDA          a CUDA runtime or driver call failed (no device, launch error).

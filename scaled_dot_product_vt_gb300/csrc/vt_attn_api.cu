@@ -33,7 +33,9 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 namespace {
 
 constexpr int64_t kMaxD = 128;
-constexpr int64_t kMaxExtent = 0x7FFFFFFF;
+constexpr int64_t kMaxExtent = 0x7FFFFFFF;  // B and H (their product is bounded by the work-unit count)
+// S_q and S_k: the kernels form row and key indices a few tiles past an extent in 32-bit ints
+constexpr int64_t kMaxSeq = int64_t(1) << 30;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 constexpr int kSmemLimit = 232448;  // 227 KiB per CTA on sm_100-class parts
 
@@ -403,7 +405,7 @@ vt_status check_args(const Problem &P, bool *empty) {
     if (windowed && P.window < 1) return VT_ERR_INVALID_ARG;
     if (P.offset > vt::kMaxBandArg || (windowed && P.window > vt::kMaxBandArg)) return VT_ERR_UNSUPPORTED;
     if (D_qk > vt::kMaxD || D_v > vt::kMaxD) return VT_ERR_UNSUPPORTED;
-    if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxExtent || S_k > vt::kMaxExtent)
+    if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxSeq || S_k > vt::kMaxSeq)
         return VT_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || S_q == 0) {
         *empty = true;

@@ -53,6 +53,7 @@ def call(B=1, H=1, S_q=4, S_k=4, D_qk=8, D_v=8, scale=0.5, causal=0, dtype=vt.VT
     (dict(B=-1), 1), (dict(H=-2), 1), (dict(S_q=-1), 1), (dict(S_k=-5), 1),
     (dict(dtype=7), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(D_qk=129), 2), (dict(D_v=256), 2), (dict(S_q=1 << 31), 2),
+    (dict(S_q=(1 << 30) + 1), 2), (dict(S_k=(1 << 30) + 1), 2), (dict(B=1 << 31), 2), (dict(H=1 << 31), 2),
     (dict(ptrs=(A, 2 * A, 3 * A, 0)), 1), (dict(ptrs=(0, 2 * A, 3 * A, 4 * A)), 1),
     (dict(ptrs=(A + 8, 2 * A, 3 * A, 4 * A)), 3), (dict(ptrs=(A, 2 * A, 3 * A, 4 * A + 2)), 3),
     (dict(D_qk=4, dtype=vt.VT_BF16), 3),        # row pitch 8 bytes: not a TMA stride
