@@ -4,8 +4,10 @@
 A step is one vt_attn_fwd call over the whole workload (default: B=8, H=16,
 S_q=S_k=8192, D=128, bf16, causal, Q ~ N(0, 4^2), K, V ~ N(0, 1), seed 4).  The masked and
 grouped-head workloads (--workload bf16_gqa_causal_8k, bf16_prefill_on_cache_8k,
-bf16_window_1k_8k) call vt_attn_fwd_general instead and count 2*(D_qk+D_v) flops per
-(query, key) pair their mask keeps.
+bf16_window_1k_8k, bf16_chunk_on_cache_32k) call vt_attn_fwd_general instead and count
+2*(D_qk+D_v) flops per (query, key) pair their mask keeps.  Split-KV shares are the library's
+choice (vt_attn_splitkv_choose; --split N overrides): 1 for the default workload, more where
+the query blocks do not fill the SMs, in which case a step also runs the merge kernel.
 
   value        TFLOP/s over the timed steps, inputs resident in HBM (flops = 4*B*H*S_q*S_k*D,
                halved for causal; 2*B*H*S_q*S_k*(D_qk+D_v) in general), CUDA events on the
@@ -266,6 +268,8 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=512, help="reference arm: query rows per step")
+    ap.add_argument("--split", default="auto",
+                    help="split-KV shares: 'auto' (the library's vt_attn_splitkv_choose) or a count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -304,17 +308,26 @@ def main() -> int:
     sh = stream.cuda_stream
     flops = workload_flops(w, causal)
     mask = vt.vt_attn_mask(vt.MASKS[w.mask], 0, w.offset, w.window) if w.mask else None
+    n_split = (vt.vt_attn_splitkv_choose(w.B, w.H, w.S_q, w.S_k, int(causal), vt_dtype) if args.split == "auto"
+               else int(args.split))
+    workspace, ws_bytes = None, 0
+    if n_split > 1:
+        ws_bytes = vt.vt_attn_splitkv_workspace_size(w.B, w.H, w.S_q, w.D_v, n_split)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        if mask is None:
+            mask = vt.vt_attn_mask(vt.MASKS["causal" if causal else "none"], 0, 0, 0)
 
     def call(q_, k_, v_, o_, stream_handle):
-        """One forward through the C ABI: vt_attn_fwd, or the general entry point for masked or
-        grouped-head workloads."""
+        """One forward through the C ABI: vt_attn_fwd, or the general entry point for masked,
+        grouped-head or split-KV runs (its launches run on one stream, so one workspace serves)."""
         if mask is None:
             return vt.vt_attn_fwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), w.B, w.H, w.S_q,
                                   w.S_k, w.D_qk, w.D_v, w.scale, int(causal), vt_dtype, stream_handle)
         return vt.vt_attn_fwd_general(q_.data_ptr(), q_.stride()[:3], k_.data_ptr(), k_.stride()[:3],
                                       v_.data_ptr(), v_.stride()[:3], o_.data_ptr(), o_.stride()[:3], None, w.B,
-                                      w.H, w.kv_heads, w.S_q, w.S_k, w.D_qk, w.D_v, w.scale, vt_dtype, mask, 1,
-                                      None, 0, None, stream_handle)
+                                      w.H, w.kv_heads, w.S_q, w.S_k, w.D_qk, w.D_v, w.scale, vt_dtype, mask, n_split,
+                                      workspace.data_ptr() if workspace is not None else None, ws_bytes, None,
+                                      stream_handle)
 
     def step():
         rc = call(Q, K, V, O, sh)
@@ -423,6 +436,7 @@ def main() -> int:
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "S_q": w.S_q, "S_k": w.S_k, "D_qk": w.D_qk,
                        "D_v": w.D_v, "causal": causal, "mode": mode_of(w, causal), "H_kv": w.kv_heads,
+                       "n_split": n_split,
                        "flops_per_step": flops,
                        "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -432,12 +446,14 @@ def main() -> int:
                          "peak_source": (f"{peaks['source']} bf16 burst" if w.dtype == "bf16"
                                          else f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio"),
                          "kernel": "vt::attn_fwd_bf16_2q_kernel" if w.dtype == "bf16" else "vt::attn_fwd_kernel<0>",
-                         "launch_ms": per_launch_ms},
+                         "launch_ms": per_launch_ms,  # one call: the attention kernel (+ the merge if split)
+                         "merge_kernel": "vt::attn_merge_kernel" if n_split > 1 else None},
             "cpu_baseline": cpu,
             "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                     "ms_per_step": e2e_ms / args.steps, "pipelined": True},
-            "gpu_launches": world * args.steps,  # kernel-only timed region: one launch per step and rank
+            # kernel-only timed region: per step and rank one attention launch, plus the merge when split
+            "gpu_launches": world * args.steps * (2 if n_split > 1 else 1),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
         }
         print(json.dumps(line), flush=True)

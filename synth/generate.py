@@ -204,6 +204,9 @@ WORKLOADS = {
                                          "normal", 1.0, 1.0, 6, mask="causal", offset=7168),
     "bf16_window_1k_8k": Workload("bf16_window_1k_8k", 8, 16, 8192, 8192, 128, 128, "bf16", (True,), "normal",
                                   1.0, 1.0, 7, mask="window", window=1024),
+    # a 256-query chunk at the end of a 32k-key cache: 32 query blocks for the whole GPU (split-KV's case)
+    "bf16_chunk_on_cache_32k": Workload("bf16_chunk_on_cache_32k", 2, 16, 256, 32768, 128, 128, "bf16", (True,),
+                                        "normal", 1.0, 1.0, 8, mask="causal", offset=32512),
 }
 
 

@@ -165,22 +165,29 @@ def test_empty_rows_written_and_guard_bands_kept(dtype):
 # ---------------------------------------------------------------- full-size shapes, sampled rows
 
 SAMPLED = {
-    # name: B, H, H_kv, S_q, S_k, D, mask, offset, window
-    "gqa_causal_4k": (8, 32, 8, 4096, 4096, 128, "causal", 0, 0),
-    "prefill_on_cache_8k": (8, 16, 16, 1024, 8192, 128, "causal", 7168, 0),
-    "window_1024_8k": (4, 16, 16, 8192, 8192, 128, "window", 0, 1024),
-    "complement_1024_8k": (2, 16, 4, 8192, 8192, 128, "window_complement", 0, 1024),
+    # name: B, H, H_kv, S_q, S_k, D, mask, offset, window, n_split (0: the library's choice)
+    "gqa_causal_4k": (8, 32, 8, 4096, 4096, 128, "causal", 0, 0, 1),
+    "prefill_on_cache_8k": (8, 16, 16, 1024, 8192, 128, "causal", 7168, 0, 1),
+    "window_1024_8k": (4, 16, 16, 8192, 8192, 128, "window", 0, 1024, 1),
+    "complement_1024_8k": (2, 16, 4, 8192, 8192, 128, "window_complement", 0, 1024, 1),
+    # the 32k-cache chunk workload, with the library's share count (4 on 152 SMs) and without shares
+    "chunk_on_cache_32k_split": (2, 16, 16, 256, 32768, 128, "causal", 32512, 0, 0),
+    "chunk_on_cache_32k_one": (2, 16, 16, 256, 32768, 128, "causal", 32512, 0, 1),
 }
 
 
 @pytest.mark.parametrize("name", sorted(SAMPLED))
 def test_full_size_sampled(name):
-    B, H, H_kv, S_q, S_k, D, mask, offset, window = SAMPLED[name]
+    B, H, H_kv, S_q, S_k, D, mask, offset, window, n_split = SAMPLED[name]
+    if n_split == 0:
+        n_split = vt.vt_attn_splitkv_choose(B, H, S_q, S_k, 1, vt.VT_BF16)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert n_split == max(1, min(sms // (B * H * ((S_q + 255) // 256)), (S_k + 127) // 128 // 4, 64))
     q, k, v = inputs("bf16", B, H, H_kv, S_q, S_k, D, D, seed=80 + len(name))
     scale = float(np.float32(1.0 / math.sqrt(D)))
-    got, lse = run_general(q, k, v, scale, mask, offset, window)
+    got, lse = run_general(q, k, v, scale, mask, offset, window, n_split)
     rng = np.random.default_rng(81)
-    edges = [0, 1, 127, 128, 255, 256, S_q // 2, S_q - 129, S_q - 1]
+    edges = [e for e in (0, 1, 127, 128, 255, 256, S_q // 2, S_q - 129, S_q - 1) if 0 <= e < S_q]
     rows = sorted({(int(b), int(h), int(i)) for b, h in [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]
                    for i in edges + [int(x) for x in rng.integers(0, S_q, size=24)]})
     rows = np.array(rows, dtype=np.int64)
