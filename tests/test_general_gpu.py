@@ -173,6 +173,9 @@ SAMPLED = {
     # the 32k-cache chunk workload, with the library's share count (4 on 152 SMs) and without shares
     "chunk_on_cache_32k_split": (2, 16, 16, 256, 32768, 128, "causal", 32512, 0, 0),
     "chunk_on_cache_32k_one": (2, 16, 16, 256, 32768, 128, "causal", 32512, 0, 1),
+    # long and wide extremes: 2^20 keys (8192 key tiles; 38 shares on 152 SMs), and 4096 heads
+    "long_cache_1m_split": (1, 2, 2, 300, 1 << 20, 128, "causal", (1 << 20) - 300, 0, 0),
+    "many_heads_4096": (64, 64, 16, 256, 256, 64, "none", 0, 0, 1),
 }
 
 
@@ -182,7 +185,8 @@ def test_full_size_sampled(name):
     if n_split == 0:
         n_split = vt.vt_attn_splitkv_choose(B, H, S_q, S_k, 1, vt.VT_BF16)
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        assert n_split == max(1, min(sms // (B * H * ((S_q + 255) // 256)), (S_k + 127) // 128 // 4, 64))
+        items = B * H * ((S_q + 255) // 256)
+        assert n_split == max(1, min(sms // items if items < sms else 1, (S_k + 127) // 128 // 4, 64))
     q, k, v = inputs("bf16", B, H, H_kv, S_q, S_k, D, D, seed=80 + len(name))
     scale = float(np.float32(1.0 / math.sqrt(D)))
     got, lse = run_general(q, k, v, scale, mask, offset, window, n_split)
