@@ -105,8 +105,19 @@ vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3],
  *   flags            VT_OPT_TEST_STALL makes the kernel wait on a barrier that is never
  *                    signalled, so that the time-limit path can be tested; it does no
  *                    attention work and leaves O unwritten.
+ *                    VT_OPT_TEST_BOUNDS (debug library only, libvt_attn_debug.so, built
+ *                    with VT_DEBUG) makes the first device index check of the producer
+ *                    report a failure, so that the VT_ERR_DEVICE_BOUNDS path can be tested:
+ *                    the kernel stops before any access and leaves O unwritten.  The
+ *                    release library ignores it.
+ *
+ * The debug library exports the same entry points.  Its kernels check their index invariants
+ * (decoded work units, key-tile ranges, ring slots, output rows) before each access they guard;
+ * a failed check records VT_ERR_DEVICE_BOUNDS for vt_last_device_status, skips the access and
+ * stops the kernel through the same clean path as a time-out.
  */
 #define VT_OPT_TEST_STALL 1u
+#define VT_OPT_TEST_BOUNDS 2u
 typedef struct {
     uint64_t wait_timeout_ns;
     uint32_t flags;

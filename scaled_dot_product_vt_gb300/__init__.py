@@ -11,10 +11,11 @@ from __future__ import annotations
 import ctypes
 import os
 
-from ._build import LIB, build  # noqa: F401
+from ._build import LIB, LIB_DEBUG, build  # noqa: F401
 
 VT_F32, VT_BF16 = 0, 1
 VT_OPT_TEST_STALL = 1
+VT_OPT_TEST_BOUNDS = 2
 VT_MASK_NONE, VT_MASK_CAUSAL, VT_MASK_WINDOW, VT_MASK_WINDOW_COMPLEMENT = 0, 1, 2, 3
 MASKS = {"none": VT_MASK_NONE, "causal": VT_MASK_CAUSAL, "window": VT_MASK_WINDOW,
          "window_complement": VT_MASK_WINDOW_COMPLEMENT}
@@ -87,6 +88,13 @@ def load(path: str | None = None):
     if path is None:
         _lib = lib
     return lib
+
+
+def load_debug():
+    """Load libvt_attn_debug.so: the same entry points, with device index checks (VT_DEBUG) that report
+    VT_ERR_DEVICE_BOUNDS.  Returns a separate handle; the module-level wrappers keep using the release
+    library."""
+    return load(LIB_DEBUG)
 
 
 def _stride3(s):

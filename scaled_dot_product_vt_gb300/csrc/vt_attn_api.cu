@@ -12,6 +12,8 @@
 #include <cstdlib>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/vt_attn.h"
 #include "vt_attn_bf16_2q.cuh"
 #include "vt_attn_kernel.cuh"
@@ -31,6 +33,15 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
+
+// An NVTX range over one public call (named after the entry point), for profilers that record NVTX;
+// without one attached, push and pop return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr int64_t kMaxD = 128;
 constexpr int64_t kMaxExtent = 0x7FFFFFFF;  // B and H (their product is bounded by the work-unit count)
@@ -383,7 +394,10 @@ const char *vt_status_str(vt_status s) {
     return "unknown vt_status";
 }
 
-vt_status vt_last_device_status(vt_stream_t stream) { return vt::read_status(reinterpret_cast<cudaStream_t>(stream)); }
+vt_status vt_last_device_status(vt_stream_t stream) {
+    const vt::NvtxRange range("vt_last_device_status");
+    return vt::read_status(reinterpret_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"
 
@@ -492,6 +506,7 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3], const void *K
                          const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
                          int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
                          vt_dtype dtype, const vt_attn_opts *opts, vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd_ex");
     const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
                                             D_v, scale, causal, dtype);
     bool empty = false;
@@ -506,6 +521,7 @@ vt_status vt_attn_fwd_general(const void *Q, const int64_t q_stride[3], const vo
                               int64_t D_v, float scale, vt_dtype dtype, const vt_attn_mask *mask, int n_split,
                               void *workspace, size_t workspace_bytes, const vt_attn_opts *opts,
                               vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd_general");
     vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v,
                                       scale, 0, dtype);
     P.H_kv = H_kv;
@@ -558,6 +574,7 @@ vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3], const vo
                               int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
                               vt_dtype dtype, int n_split, void *workspace, size_t workspace_bytes,
                               vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd_splitkv");
     const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
                                             D_v, scale, causal, dtype);
     bool empty = false;
@@ -578,6 +595,7 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], 
                                       const int64_t o_stride[3], int64_t B, int64_t H, int64_t S_q, int64_t S_k,
                                       int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype, int n_split,
                                       vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd_splitkv_noalloc");
     const vt::Problem P = vt::plain_problem(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk,
                                             D_v, scale, causal, dtype);
     bool empty = false;
@@ -602,6 +620,7 @@ vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const vo
                               const void *V, const int64_t v_stride[3], void *O, const int64_t o_stride[3], int64_t B,
                               int64_t H, int64_t S_q, int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal,
                               vt_dtype dtype, vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd_strided");
     return vt_attn_fwd_ex(Q, q_stride, K, k_stride, V, v_stride, O, o_stride, B, H, S_q, S_k, D_qk, D_v, scale,
                           causal, dtype, nullptr, stream);
 }
@@ -609,6 +628,7 @@ vt_status vt_attn_fwd_strided(const void *Q, const int64_t q_stride[3], const vo
 vt_status vt_attn_fwd(const void *Q, const void *K, const void *V, void *O, int64_t B, int64_t H, int64_t S_q,
                       int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype,
                       vt_stream_t stream) {
+    const vt::NvtxRange range("vt_attn_fwd");
     const int64_t qs[3] = {H * S_q * D_qk, S_q * D_qk, D_qk};
     const int64_t ks[3] = {H * S_k * D_qk, S_k * D_qk, D_qk};
     const int64_t vs[3] = {H * S_k * D_v, S_k * D_v, D_v};

@@ -154,6 +154,15 @@ __device__ __forceinline__ Unit decode_unit(const AttnParams &p, int u) {
     return U;
 }
 
+// Invariants of a decoded unit, checked by the debug build before the unit's loads are issued.
+__device__ __forceinline__ bool unit_valid(const AttnParams &p, const Unit &U) {
+    const int tiles = (p.S_k + kBN - 1) / kBN;
+    return U.b >= 0 && U.b < p.B && U.h >= 0 && U.h < p.H && U.hk == U.h / p.kv_group && U.r0 >= 0 &&
+           U.r0 < p.S_q && U.r0 % kRows == 0 && U.split >= 0 && U.split < p.n_split && U.j0 >= 0 && U.n_kv >= 0 &&
+           U.j0 + U.n_kv <= tiles && U.as0 >= 0 && U.as0 <= U.es0 && U.es0 <= U.n_kv && U.as1 >= 0 &&
+           U.as1 <= U.es1 && U.es1 <= U.n_kv;
+}
+
 // The n-th unit this CTA works on, as the producer decoded and published it (u = -1: no more
 // units); false on abort.  Called by a whole warp: lane 0 waits for the ring entry and releases it,
 // every lane copies the unit (the producer decodes ahead, so readers spend no time on it).
@@ -265,6 +274,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 Unit U;
                 if (u >= 0) {
                     U = decode_unit(p, u);
+                    if (!VT_DEV_CHECK(!(p.flags & kFlagTestBounds) && unit_valid(p, U), ctl.abort_flag, p)) break;
                 } else {
                     U.u = -1;
                     U.split = U.b = U.h = U.hk = U.r0 = U.j0 = U.n_kv = U.as0 = U.es0 = U.as1 = U.es1 = 0;
@@ -308,6 +318,10 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     const uint32_t dst = sSlot0 + s * slot_bytes;
                     const uint32_t bar = smem_u32(&ctl.full[s]);
                     const int j = i >> 1;
+                    if (!VT_DEV_CHECK(s < n_slots && (U.j0 + j) * BN < p.S_k, ctl.abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
                     if ((i & 1) == 0) {
                         mbar_arrive_expect_tx(bar, k_bytes);
                         for (int c = 0; c < p.q_chunks; ++c)
@@ -377,7 +391,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     mma_ts_elect(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u);
             };
 
-            if (p.flags & 1u) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
+            if (p.flags & kFlagTestStall) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
             int ks = 0;  // slot of the next K tile (the ring runs on across units)
             for (int n = 0; ok; ++n) {
                 Unit U;

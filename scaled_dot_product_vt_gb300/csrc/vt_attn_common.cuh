@@ -100,6 +100,25 @@ __device__ __forceinline__ float lse_from(float m, float l) {
     return l > 0.0f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
 }
 
+// Device index checks of the debug build (-DVT_DEBUG): a failed check records the bounds bit of the
+// status word and the CTA's abort flag, and the caller skips the access it guards and stops.  Release
+// builds compile the checks out (the condition is not evaluated).
+#ifdef VT_DEBUG
+#define VT_DEV_CHECK(cond, abort_flag, p) ::vt::dev_check((cond), (abort_flag), (p))
+#else
+#define VT_DEV_CHECK(cond, abort_flag, p) true
+#endif
+constexpr unsigned kFlagTestStall = 1u;   // VT_OPT_TEST_STALL
+constexpr unsigned kFlagTestBounds = 2u;  // VT_OPT_TEST_BOUNDS (debug build)
+
+__device__ __forceinline__ bool dev_check(bool ok, volatile uint32_t &abort_flag, const AttnParams &p) {
+    if (!ok) {
+        abort_flag = 1;
+        atomicOr(p.status, kStatusBounds);
+    }
+    return ok;
+}
+
 // Wait for the phase of `bar` with `parity`, giving up after the time limit or when
 // another role has aborted.  Returns false on give-up (after flagging the abort).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t &abort_flag,

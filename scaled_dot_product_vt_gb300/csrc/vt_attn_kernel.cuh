@@ -111,6 +111,12 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
     const int share_lo = min(split * per, n_all);
     j_first += share_lo;
     const int n_kv = min(n_all, share_lo + per) - share_lo;
+    // (checked by the debug build before any load of the item)
+    auto item_valid = [&]() {
+        return split >= 0 && split < p.n_split && qb >= 0 && qb < p.n_qblocks && b >= 0 && b < p.B && h >= 0 &&
+               h < p.H && hk == h / p.kv_group && q_row0 < p.S_q && j_first >= 0 && n_kv >= 0 &&
+               j_first + n_kv <= (p.S_k + BN - 1) / BN;
+    };
 
     // Shared-memory carve-up (1024-byte aligned for the 128-byte swizzle).
     const uint32_t raw = smem_u32(smem_raw);
@@ -156,7 +162,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0 && n_kv > 0 &&
+            VT_DEV_CHECK(!(p.flags & kFlagTestBounds) && item_valid(), ctl.abort_flag, p)) {  // else nothing issued
             mbar_arrive_expect_tx(smem_u32(&ctl.q_full), q_bytes);
             for (int c = 0; c < p.q_chunks; ++c)
                 tma_load_4d(sQ + c * kBM * 128, &tmQ, smem_u32(&ctl.q_full), c * C::kChunkElems, q_row0, h, b);
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
             auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl.abort_flag, p)) != 0;
             };
-            if (p.flags & 1u) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook: never signalled
+            if (p.flags & kFlagTestStall) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook: never signalled
             if (ok) ok = wait1(smem_u32(&ctl.q_full), 0);
 
             auto issue_qk = [&](int j) -> bool {
@@ -260,7 +267,8 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
         const float *vbh = static_cast<const float *>(p.V) + static_cast<long long>(b) * p.v_sb +
                            static_cast<long long>(hk) * p.v_sh;
         uint8_t *smem_gen = smem_raw + (base - raw);
-        for (int j = group; j < n_kv; j += C::kVLoaderGroups) {
+        const bool loads_ok = VT_DEV_CHECK(item_valid(), ctl.abort_flag, p);
+        for (int j = group; loads_ok && j < n_kv; j += C::kVLoaderGroups) {
             const int st = j % p.stages;
             const int use = j / p.stages;
             if (use > 0) {

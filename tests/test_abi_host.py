@@ -34,6 +34,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_debug_library_exports_every_declared_symbol(lib):
+    dbg = vt.load_debug()
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    # host-side checks are shared: the same argument error before any launch
+    assert dbg.vt_attn_fwd(1 << 20, 2 << 20, 3 << 20, 4 << 20, 1, 1, 4, 0, 8, 8, 0.5, 0, vt.VT_BF16, None) == 1
+
+
 def test_status_strings(lib):
     for code, name in vt.STATUS.items():
         assert vt.vt_status_str(code).startswith(name)
