@@ -32,6 +32,7 @@ import argparse
 import dataclasses
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -189,29 +190,48 @@ def mode_of(w, causal: bool) -> str:
     return f"mask {w.mask}{extra}{heads}"
 
 
-def cpu_oracle_sample(w, q, k, v, causal: bool, target_s: float = 12.0, max_slices: int = 32):
-    """Time the fp64 oracle on whole (b, h) slices of the workload until ~target_s seconds have passed."""
+# parity bars of the element types: (max abs, relative Frobenius or None)
+TOLERANCE = {"bf16": (2e-2, 1e-2), "f32": (5e-3, None)}
+
+
+def cpu_oracle_sample(w, q, k, v, causal: bool, target_s: float = 12.0, max_slices: int = 32, gpu_slice=None):
+    """Time the fp64 oracle on whole (b, h) slices of the workload until ~target_s seconds have passed.
+    With gpu_slice(b, h) -> the GPU's output of that slice (fp64), also return the parity of the sampled
+    slices (compared outside the timed part)."""
     import oracle
     nthreads = oracle.default_threads()
     rows_per_slice = w.S_q
     done_flops, t_total, slices = 0.0, 0.0, 0
+    max_abs, err2, ref2 = 0.0, 0.0, 0.0
     for s in range(max_slices):
         b, h = divmod(s, w.H)
         b %= w.B
         rows = np.stack([np.full(rows_per_slice, b), np.full(rows_per_slice, h), np.arange(rows_per_slice)], axis=1)
         t0 = time.perf_counter()
         if w.mask:
-            oracle.attn_general(q, k, v, w.scale, w.mask, w.offset, w.window, rows=rows, nthreads=nthreads)
+            ref = oracle.attn_general(q, k, v, w.scale, w.mask, w.offset, w.window, rows=rows, nthreads=nthreads)
         else:
-            oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
+            ref = oracle.attn_rows(q, k, v, w.scale, causal, rows, nthreads=nthreads)
         t_total += time.perf_counter() - t0
+        if gpu_slice is not None:
+            d = gpu_slice(b, h) - np.asarray(ref, dtype=np.float64).reshape(w.S_q, w.D_v)
+            max_abs = max(max_abs, float(np.abs(d).max()))
+            err2 += float((d * d).sum())
+            ref2 += float((np.asarray(ref, dtype=np.float64) ** 2).sum())
         done_flops += workload_flops(w, causal) / (w.B * w.H)
         slices += 1
         if t_total >= target_s:
             break
-    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{slices} whole (b,h) slice(s) of {w.name} ({w.S_q} rows each, {mode_of(w, causal)}), "
-                      f"{t_total:.1f} s fp64 on {nthreads} host threads"}
+    out = {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+           "sample": f"{slices} whole (b,h) slice(s) of {w.name} ({w.S_q} rows each, {mode_of(w, causal)}), "
+                     f"{t_total:.1f} s fp64 on {nthreads} host threads"}
+    if gpu_slice is not None:
+        tol_abs, tol_rel = TOLERANCE[w.dtype]
+        rel = math.sqrt(err2 / ref2) if ref2 > 0 else 0.0
+        out["parity"] = {"slices": slices, "max_abs": max_abs, "rel_fro": rel, "tol_max_abs": tol_abs,
+                         "tol_rel_fro": tol_rel,
+                         "pass": max_abs <= tol_abs and (tol_rel is None or rel <= tol_rel)}
+    return out
 
 
 def run_reference(args, w, causal):
@@ -438,7 +458,9 @@ def main() -> int:
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_oracle_sample(w, q, k, v, causal, target_s=args.cpu_seconds)
+            # O holds the result of the timed steps (the end-to-end steps rewrote it from the same inputs)
+            cpu = cpu_oracle_sample(w, q, k, v, causal, target_s=args.cpu_seconds,
+                                    gpu_slice=lambda b, h: O[b, h].double().cpu().numpy())
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
