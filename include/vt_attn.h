@@ -137,7 +137,8 @@ vt_status vt_attn_fwd_ex(const void *Q, const int64_t q_stride[3],
 /*
  * Split-KV forward: the same operation, with the key range of every query block cut into
  * n_split contiguous shares that separate CTAs process at the same time.  Each share writes an
- * unnormalised partial output with its row max and row sum to `workspace`; a merge kernel then
+ * unnormalised partial output with its row max, its row sum and that sum's correction for the
+ * bf16 rounding of P (bf16 I/O) to `workspace`; a merge kernel then
  * combines the shares of each row into O (the continuation step of the VeriTile coverage table's
  * attention_fwd_triton3 row, case 4, which reads a previous M, L and Out and merges further keys).
  * It pays off when B * H * ceil(S_q / 256) is below the number of SMs (long keys, few queries).

@@ -161,7 +161,7 @@ bool make_map(CUtensorMap *map, const void *ptr, const int64_t st[3], int64_t B,
 
 // Workspace of a split-KV call: partial outputs, then row maxima, then row sums (256-byte aligned).
 struct SplitLayout {
-    size_t o_off, m_off, l_off, bytes;
+    size_t o_off, m_off, l_off, c_off, bytes;
 };
 SplitLayout split_layout(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split) {
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -170,7 +170,8 @@ SplitLayout split_layout(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_s
     L.o_off = 0;
     L.m_off = up(static_cast<size_t>(n_split) * rows * D_v * sizeof(float));
     L.l_off = L.m_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
-    L.bytes = L.l_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
+    L.c_off = L.l_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
+    L.bytes = L.c_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
     return L;
 }
 
@@ -206,6 +207,7 @@ vt_status merge(const AttnParams &p, const Problem &P, cudaStream_t stream) {
     mp.part_o = p.part_o;
     mp.part_m = p.part_m;
     mp.part_l = p.part_l;
+    mp.part_c = p.part_c;
     mp.O = P.O;
     mp.lse = P.lse;
     mp.rows = P.B * P.H * P.S_q;
@@ -272,6 +274,7 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         p.part_o = reinterpret_cast<float *>(ws + L.o_off);
         p.part_m = reinterpret_cast<float *>(ws + L.m_off);
         p.part_l = reinterpret_cast<float *>(ws + L.l_off);
+        p.part_c = reinterpret_cast<float *>(ws + L.c_off);
     }
     p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : kDefaultTimeoutNs;
     p.flags = opts ? opts->flags : 0u;

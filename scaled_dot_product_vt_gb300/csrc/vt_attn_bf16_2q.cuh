@@ -494,6 +494,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             const int mask_hi = band_key_hi(p, tile_row0);
             float m_used = -INFINITY;  // reference max (log2 units) of O_t and l
             float l = 0.0f;
+            float l_fix = 0.0f;        // bf16 rounding of each tile's largest P, relative to m_used
 
             for (int j = 0; j < n_my; ++j) {
                 ok = wait_bounded(smem_u32(&ctl.s_full[t]), s_par, ctl.abort_flag, p);
@@ -529,7 +530,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
                 mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
                 mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;  // c > 0: -inf stays -inf
+                const float m_raw = fmax3(fmaxf(mx0, mx1), mx2, mx3);
+                const float m_tile = m_raw * c;  // c > 0: -inf stays -inf
                 const float m_new = fmaxf(m_used, m_tile);
                 // Lazy rescale: keep the old reference unless the max grew by more than tau.
                 const bool resc = (m_used == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_used > kTau);
@@ -537,10 +539,17 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 if (resc) {
                     alpha = (m_used == -INFINITY) ? 0.0f : ex2(m_used - m_new);
                     l *= alpha;
+                    l_fix *= alpha;
                     m_used = m_new;
                 }
                 const float m_ref = (m_used == -INFINITY) ? 0.0f : m_used;
                 const float2 nm2 = make_float2(-m_ref, -m_ref);
+                // P V multiplies P rounded to bf16, while l adds the fp32 values.  The tile's largest P,
+                // formed exactly as below, gives its rounding error to l_fix, and O is divided by l + l_fix:
+                // a key that dominates its row then carries the same weight in both (exact when one key
+                // dominates).  The log-sum-exp uses l alone.
+                const float p_top = ex2(__fmaf_rn(m_raw, c, -m_ref));
+                l_fix += __uint_as_float(pack_bf16x2(p_top, 0.0f) << 16) - p_top;
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
                 // P_t,j over S_t,j (bf16 pairs): each 32-score chunk goes to TMEM as 16 columns as
                 // soon as it is exponentiated, which keeps the live registers near the 128 scores.
@@ -589,7 +598,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 // ------------------------------------------------------------ epilogue: O = O_t / l
                 // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
                 if (n_my > 0) tc_fence_after();
-                const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+                const float inv_l = l > 0.0f ? 1.0f / (l + l_fix) : 0.0f;
                 uint8_t *orow = reinterpret_cast<uint8_t *>(p.O) +
                                 (static_cast<long long>(U.b) * p.o_sb + static_cast<long long>(U.h) * p.o_sh +
                                  static_cast<long long>(q_row) * p.o_ss) * 2;
@@ -653,6 +662,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 if (row_ok) {
                     p.part_m[part] = n_my > 0 ? m_used : -INFINITY;
                     p.part_l[part] = n_my > 0 ? l : 0.0f;
+                    p.part_c[part] = n_my > 0 ? l_fix : 0.0f;
                 }
             }
         }

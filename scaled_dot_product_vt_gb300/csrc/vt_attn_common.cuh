@@ -45,11 +45,13 @@ struct AttnParams {
     long long v_sb, v_sh, v_ss;
     // Split-KV: each work item's key tiles are cut into n_split contiguous ranges, one per CTA; with
     // n_split > 1 the CTAs write unnormalised partial outputs (fp32, D_v per row), their row max m
-    // (log2 units, -inf if no allowed key) and row sum l, indexed [split][(b*H + h)*S_q + i].
+    // (log2 units, -inf if no allowed key), row sum l and the correction that makes l + corr weigh P
+    // as the bf16 values P V used, indexed [split][(b*H + h)*S_q + i].
     int n_split;
     float *part_o;
     float *part_m;
     float *part_l;
+    float *part_c;
     unsigned long long timeout_ns;
     unsigned flags;
     unsigned *status;  // device status word

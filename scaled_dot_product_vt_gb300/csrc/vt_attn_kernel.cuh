@@ -485,6 +485,7 @@ __global__ void __launch_bounds__(Cfg<DT>::kThreads, 1)
                 if (row_ok) {
                     p.part_m[part] = n_kv > 0 ? m_used : -INFINITY;
                     p.part_l[part] = n_kv > 0 ? l : 0.0f;
+                    p.part_c[part] = 0.0f;  // P stays fp32 here: no bf16 rounding to weigh
                 }
             } else {
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;

@@ -19,6 +19,7 @@ struct MergeParams {
     const float *part_o;
     const float *part_m;
     const float *part_l;
+    const float *part_c;
     void *O;
     float *lse;      // nullptr, or one natural-log log-sum-exp per row
     long long rows;  // B * H * S_q
@@ -37,13 +38,15 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
     if (row >= mp.rows) return;
     float M = -INFINITY;
     for (int s = 0; s < mp.n_split; ++s) M = fmaxf(M, mp.part_m[s * mp.rows + row]);
-    float L = 0.0f;
+    float L = 0.0f;   // sum of the shares' l: the log-sum-exp
+    float Lo = 0.0f;  // sum of l + corr: the divisor of O, weighing P as P V used it
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < mp.n_split; ++s) {
         const float ms = mp.part_m[s * mp.rows + row];
         if (ms == -INFINITY) continue;  // no allowed key in this share
         const float w = ex2(ms - M);
         L += w * mp.part_l[s * mp.rows + row];
+        Lo += w * (mp.part_l[s * mp.rows + row] + mp.part_c[s * mp.rows + row]);
         const float *po = mp.part_o + (s * mp.rows + row) * mp.D_v;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -51,7 +54,7 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
             if (col < mp.D_v) acc[c] += w * po[col];
         }
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;  // no share saw an allowed key: the row is 0
+    const float inv = L > 0.0f ? 1.0f / Lo : 0.0f;  // no share saw an allowed key: the row is 0
     if (mp.lse && lane == 0) mp.lse[row] = lse_from(M, L);
     const long long i = row % mp.S_q;
     const long long bh = row / mp.S_q;

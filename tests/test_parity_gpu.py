@@ -217,3 +217,32 @@ def test_stalled_pipeline_reports_timeout_and_context_survives():
     got = to_host64(vt.attn_fwd(Q, K, V, scale=0.125))
     assert vt.vt_last_device_status() == 0
     check(got, oracle.attn_fwd(q, k, v, 0.125, False), "bf16", "after timeout")
+
+
+def test_rows_dominated_by_one_key_reproduce_its_value_row():
+    """Where one key carries all but ~1e-4 of a row's weight, the output must round to that key's V values:
+    P V multiplies the dominant P rounded to bf16, and the row sum has to weigh it the same way (a mismatch
+    of up to 2^-9 moves the result by up to half a bf16 step).  Checked on every element whose exact value
+    lies within a quarter bf16 step of the dominant key's value."""
+    B, H, S, D = 1, 4, 1024, 128
+    q, k, v = synth.make_qkv(B, H, S, S, D, D, "bf16", sigma_q=40.0, seed=77)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    got = vt.attn_fwd(to_device(q), to_device(k), to_device(v), scale=scale, causal=False)
+    assert vt.vt_last_device_status() == 0
+    got = got.double().cpu().numpy()
+    qf, kf, vf = (synth.bf16_bits_to_fp32(a).astype(np.float64) for a in (q, k, v))
+    checked = 0
+    for h in range(H):
+        s = scale * qf[0, h] @ kf[0, h].T
+        w = np.exp(s - s.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        exact = w @ vf[0, h]
+        top = w.argmax(axis=1)
+        vtop = vf[0, h][top]
+        step = np.ldexp(1.0, np.frexp(vtop)[1] - 8)  # bf16 spacing at |vtop|
+        sel = ((w[np.arange(S), top] > 1.0 - 1e-4)[:, None] & (np.abs(vtop) >= 1e-2)
+               & (np.abs(exact - vtop) <= 0.25 * step))
+        checked += int(sel.sum())
+        bad = np.nonzero(sel & (got[0, h] != vtop))
+        assert bad[0].size == 0, f"head {h}: {bad[0].size} elements of dominated rows are off their key's value"
+    assert checked > B * H * S * D // 4, f"only {checked} elements checked"
