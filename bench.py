@@ -190,6 +190,11 @@ def mode_of(w, causal: bool) -> str:
     return f"mask {w.mask}{extra}{heads}"
 
 
+def needs_l2_flush(in_bytes: int, out_bytes: int, l2_bytes: int) -> bool:
+    """True when a step's inputs and output could stay in L2 between timed steps (under twice its size)."""
+    return in_bytes + out_bytes < 2 * l2_bytes
+
+
 # parity bars of the element types: (max abs, relative Frobenius or None)
 TOLERANCE = {"bf16": (2e-2, 1e-2), "f32": (5e-3, None)}
 
@@ -362,7 +367,8 @@ def main() -> int:
     in_bytes = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
     out_bytes = hO.numel() * hO.element_size()
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
-    flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev) if in_bytes + out_bytes < 2 * l2_bytes else None
+    flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev) if needs_l2_flush(
+        in_bytes, out_bytes, l2_bytes) else None
 
     for _ in range(args.warmup):
         step()
