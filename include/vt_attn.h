@@ -41,8 +41,10 @@
  *                        an unknown dtype, a non-finite scale, O overlapping Q/K/V,
  *                        or a non-positive stride;
  *   VT_ERR_UNSUPPORTED   D_qk or D_v above 128, S_q or S_k above 2^30, B or H above
- *                        2^31 - 1, or more than 2^31 - 1 work units (query blocks x heads x
+ *                        2^31 - 1, a (b, h, s) stride of 2^40 bytes or more (beyond a TMA
+ *                        tensor map), or more than 2^31 - 1 work units (query blocks x heads x
  *                        batches x split-KV shares);
+ *   (also VT_ERR_INVALID_ARG: extents and strides whose byte span overflows 64 bits);
  *   VT_ERR_MISALIGNED    a pointer not 16-byte aligned, or a (b, h, s) stride whose
  *                        byte size is not a multiple of 16 (the TMA engine's rule);
  *   VT_ERR_CUDA          a CUDA runtime or driver call failed (no device, launch error).
@@ -162,7 +164,8 @@ vt_status vt_attn_fwd_splitkv(const void *Q, const int64_t q_stride[3],
                               int n_split, void *workspace, size_t workspace_bytes,
                               vt_stream_t stream);
 
-/* Bytes of workspace vt_attn_fwd_splitkv needs (0 when n_split <= 1 or an extent is not positive).
+/* Bytes of workspace vt_attn_fwd_splitkv needs (0 when n_split <= 1, an extent is not positive, or
+ * the size overflows: no such workspace can exist, and such a call is rejected).
  * Host-only arithmetic: no GPU call. */
 size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split);
 

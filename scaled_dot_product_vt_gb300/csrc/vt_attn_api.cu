@@ -54,11 +54,35 @@ struct Span {
     uintptr_t lo, hi;  // [lo, hi) bytes touched by a tensor's logical elements
 };
 
-Span span_of(const void *p, const int64_t st[3], int64_t B, int64_t H, int64_t S, int64_t D, int elt) {
+// The bytes a tensor's logical elements touch; false when the extent arithmetic overflows (no such
+// tensor fits in an address space).  Extents and strides are positive here.
+bool span_of(const void *p, const int64_t st[3], int64_t B, int64_t H, int64_t S, int64_t D, int elt, Span *out) {
+    const int64_t n[3] = {B - 1, H - 1, S - 1};
+    int64_t last = D - 1, t = 0, bytes = 0;
+    for (int i = 0; i < 3; ++i)
+        if (__builtin_mul_overflow(n[i], st[i], &t) || __builtin_add_overflow(last, t, &last)) return false;
+    if (__builtin_add_overflow(last, int64_t(1), &bytes) || __builtin_mul_overflow(bytes, int64_t(elt), &bytes))
+        return false;
     const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-    const int64_t last = (B - 1) * st[0] + (H - 1) * st[1] + (S - 1) * st[2] + (D - 1);
-    return {lo, lo + static_cast<uintptr_t>(last + 1) * elt};
+    if (static_cast<uint64_t>(bytes) > UINTPTR_MAX - lo) return false;
+    *out = {lo, lo + static_cast<uintptr_t>(bytes)};
+    return true;
 }
+
+// The LSE array: B * H * S_q floats from `lse`; false on overflow.
+bool lse_span(const float *lse, int64_t B, int64_t H, int64_t S_q, Span *out) {
+    int64_t n = 0;
+    if (__builtin_mul_overflow(B, H, &n) || __builtin_mul_overflow(n, S_q, &n) ||
+        __builtin_mul_overflow(n, int64_t(sizeof(float)), &n))
+        return false;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(lse);
+    if (static_cast<uint64_t>(n) > UINTPTR_MAX - lo) return false;
+    *out = {lo, lo + static_cast<uintptr_t>(n)};
+    return true;
+}
+
+// Largest (b, h, s) stride in bytes that a TMA tensor map accepts is below 2^40.
+constexpr int64_t kMaxStrideBytes = int64_t(1) << 40;
 
 bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
@@ -163,15 +187,22 @@ bool make_map(CUtensorMap *map, const void *ptr, const int64_t st[3], int64_t B,
 struct SplitLayout {
     size_t o_off, m_off, l_off, c_off, bytes;
 };
+// bytes = 0 when the sizes overflow (no such workspace can exist).
 SplitLayout split_layout(int64_t B, int64_t H, int64_t S_q, int64_t D_v, int n_split) {
-    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    const size_t rows = static_cast<size_t>(B) * H * S_q;
-    SplitLayout L;
+    auto up = [](uint64_t x) { return (x + 255) & ~uint64_t(255); };
+    SplitLayout L{};
+    uint64_t rows = 0, per = 0, o_bytes = 0;
+    if (B <= 0 || H <= 0 || S_q <= 0 || D_v <= 0 || n_split <= 0 ||
+        __builtin_mul_overflow(uint64_t(B), uint64_t(H), &rows) || __builtin_mul_overflow(rows, uint64_t(S_q), &rows) ||
+        __builtin_mul_overflow(rows, uint64_t(n_split) * sizeof(float), &per) ||
+        __builtin_mul_overflow(per, uint64_t(D_v), &o_bytes) || o_bytes > (uint64_t(1) << 60) ||
+        per > (uint64_t(1) << 60))
+        return L;
     L.o_off = 0;
-    L.m_off = up(static_cast<size_t>(n_split) * rows * D_v * sizeof(float));
-    L.l_off = L.m_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
-    L.c_off = L.l_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
-    L.bytes = L.c_off + up(static_cast<size_t>(n_split) * rows * sizeof(float));
+    L.m_off = up(o_bytes);
+    L.l_off = L.m_off + up(per);
+    L.c_off = L.l_off + up(per);
+    L.bytes = L.c_off + up(per);
     return L;
 }
 
@@ -439,16 +470,19 @@ vt_status check_args(const Problem &P, bool *empty) {
         if (reinterpret_cast<uintptr_t>(ptr) % 16) return VT_ERR_MISALIGNED;
     for (const int64_t *s : st)
         for (int i = 0; i < 3; ++i)
+            if (s[i] >= vt::kMaxStrideBytes / elt) return VT_ERR_UNSUPPORTED;
+    for (const int64_t *s : st)
+        for (int i = 0; i < 3; ++i)
             if ((s[i] * elt) % 16) return VT_ERR_MISALIGNED;
-    const vt::Span sq = vt::span_of(P.Q, P.qs, B, H, S_q, D_qk, elt);
-    const vt::Span sk = vt::span_of(P.K, P.ks, B, H_kv, S_k, D_qk, elt);
-    const vt::Span sv = vt::span_of(P.V, P.vs, B, H_kv, S_k, D_v, elt);
-    const vt::Span so = vt::span_of(P.O, P.os, B, H, S_q, D_v, elt);
+    vt::Span sq, sk, sv, so;
+    if (!vt::span_of(P.Q, P.qs, B, H, S_q, D_qk, elt, &sq) || !vt::span_of(P.K, P.ks, B, H_kv, S_k, D_qk, elt, &sk) ||
+        !vt::span_of(P.V, P.vs, B, H_kv, S_k, D_v, elt, &sv) || !vt::span_of(P.O, P.os, B, H, S_q, D_v, elt, &so))
+        return VT_ERR_INVALID_ARG;
     if (vt::overlap(so, sq) || vt::overlap(so, sk) || vt::overlap(so, sv)) return VT_ERR_INVALID_ARG;
     if (P.lse) {
         if (reinterpret_cast<uintptr_t>(P.lse) % 4) return VT_ERR_INVALID_ARG;
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(P.lse);
-        const vt::Span sl{lo, lo + static_cast<uintptr_t>(B * H * S_q) * sizeof(float)};
+        vt::Span sl;
+        if (!vt::lse_span(P.lse, B, H, S_q, &sl)) return VT_ERR_INVALID_ARG;
         if (vt::overlap(sl, sq) || vt::overlap(sl, sk) || vt::overlap(sl, sv) || vt::overlap(sl, so))
             return VT_ERR_INVALID_ARG;
     }
@@ -458,20 +492,21 @@ vt_status check_args(const Problem &P, bool *empty) {
 // Checks of a split-KV workspace (n_split > 1): present, large enough, 256-byte aligned and clear of
 // every tensor of the call.
 vt_status check_workspace(const Problem &P, int n_split, const void *workspace, size_t workspace_bytes) {
-    if (!workspace || workspace_bytes < vt::split_layout(P.B, P.H, P.S_q, P.D_v, n_split).bytes)
-        return VT_ERR_INVALID_ARG;
+    const size_t need = vt::split_layout(P.B, P.H, P.S_q, P.D_v, n_split).bytes;
+    if (!workspace || need == 0 || workspace_bytes < need) return VT_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) % 256) return VT_ERR_MISALIGNED;
     const vt::Span w{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + workspace_bytes};
     const int elt = P.dtype == VT_BF16 ? 2 : 4;
-    if (vt::overlap(w, vt::span_of(P.Q, P.qs, P.B, P.H, P.S_q, P.D_qk, elt)) ||
-        vt::overlap(w, vt::span_of(P.K, P.ks, P.B, P.H_kv, P.S_k, P.D_qk, elt)) ||
-        vt::overlap(w, vt::span_of(P.V, P.vs, P.B, P.H_kv, P.S_k, P.D_v, elt)) ||
-        vt::overlap(w, vt::span_of(P.O, P.os, P.B, P.H, P.S_q, P.D_v, elt)))
+    vt::Span sq, sk, sv, so;  // valid: check_args has passed
+    if (!vt::span_of(P.Q, P.qs, P.B, P.H, P.S_q, P.D_qk, elt, &sq) ||
+        !vt::span_of(P.K, P.ks, P.B, P.H_kv, P.S_k, P.D_qk, elt, &sk) ||
+        !vt::span_of(P.V, P.vs, P.B, P.H_kv, P.S_k, P.D_v, elt, &sv) ||
+        !vt::span_of(P.O, P.os, P.B, P.H, P.S_q, P.D_v, elt, &so))
         return VT_ERR_INVALID_ARG;
+    if (vt::overlap(w, sq) || vt::overlap(w, sk) || vt::overlap(w, sv) || vt::overlap(w, so)) return VT_ERR_INVALID_ARG;
     if (P.lse) {
-        const uintptr_t lo = reinterpret_cast<uintptr_t>(P.lse);
-        if (vt::overlap(w, vt::Span{lo, lo + static_cast<uintptr_t>(P.B * P.H * P.S_q) * sizeof(float)}))
-            return VT_ERR_INVALID_ARG;
+        vt::Span sl;
+        if (!vt::lse_span(P.lse, P.B, P.H, P.S_q, &sl) || vt::overlap(w, sl)) return VT_ERR_INVALID_ARG;
     }
     return VT_OK;
 }
@@ -610,7 +645,8 @@ vt_status vt_attn_fwd_splitkv_noalloc(const void *Q, const int64_t q_stride[3], 
     void *scratch = nullptr;
     if (n_split > 1) {
         // The shares' partial results must fit the fixed array; nothing is allocated instead.
-        if (vt::split_layout(B, H, S_q, D_v, n_split).bytes > vt::kNoAllocScratchBytes) return VT_ERR_UNSUPPORTED;
+        const size_t need = vt::split_layout(B, H, S_q, D_v, n_split).bytes;
+        if (need == 0 || need > vt::kNoAllocScratchBytes) return VT_ERR_UNSUPPORTED;
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return VT_ERR_CUDA;
         scratch = vt::noalloc_scratch(dev);

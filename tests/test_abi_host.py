@@ -103,6 +103,20 @@ def test_missing_library_fails_loudly(tmp_path):
 
 # ---------------------------------------------------------------- split-KV entry points
 
+def test_huge_strides_and_spans_are_rejected_before_launch(lib):
+    # a stride of 2^40 bytes or more is beyond a TMA tensor map
+    big = (1 << 40) // 2
+    st = (big, 64, 8)
+    assert vt.vt_attn_fwd_strided(A, st, 2 * A, (64, 64, 8), 3 * A, (64, 64, 8), 4 * A, (64, 64, 8),
+                                  2, 1, 4, 4, 8, 8, 0.5, 0, vt.VT_BF16, None) == 2
+    # strides just below that limit whose byte span overflows 64 bits: no such tensor fits in memory
+    st = (big - 8, 64, 8)
+    assert vt.vt_attn_fwd_strided(A, st, 2 * A, (64, 64, 8), 3 * A, (64, 64, 8), 4 * A, (64, 64, 8),
+                                  1 << 30, 1, 4, 4, 8, 8, 0.5, 0, vt.VT_BF16, None) == 1
+    # a workspace size that cannot exist is reported as 0
+    assert vt.vt_attn_splitkv_workspace_size(1 << 31, 1 << 31, 1 << 30, 128, 64) == 0
+
+
 def test_splitkv_workspace_size(lib):
     assert vt.vt_attn_splitkv_workspace_size(2, 3, 5, 8, 1) == 0
     assert vt.vt_attn_splitkv_workspace_size(2, 3, 5, 8, 0) == 0
