@@ -1,0 +1,67 @@
+"""A numpy model of the bf16 softmax arithmetic of one 128-key tile, checking the reasoning behind the
+row-sum correction on CPU.
+
+P V multiplies P rounded to bf16 while the row sum adds fp32 values.  In a row dominated by one key the
+output is then scaled by p_bf16 / p, off by up to 2^-9.  Added to the bf16 rounding of the output, that
+can exceed the 2e-2 bar for |O| in [4, 8).  Adding the rounding error of the tile's largest P to the sum
+makes dominated rows exact up to the output rounding.  The model: scores in fp64, exponentials in fp64
+rounded to fp32 (the kernel's ex2 is within 2 ulp of that), P rounded to bf16 with round-to-nearest-even,
+sums in fp64, output rounded to bf16.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+
+
+def _bf16(x):
+    return synth.bf16_bits_to_fp32(synth.to_bf16_bits(np.asarray(x, dtype=np.float32))).astype(np.float64)
+
+
+def _model(x, v, correct: bool, full: bool = False):
+    """Output rows for log2-unit scores x (rows x keys, reference max 0) and values v (keys x D)."""
+    p = np.exp2(x).astype(np.float32).astype(np.float64)
+    pb = _bf16(p)
+    num = pb @ v
+    if full:
+        den = pb.sum(axis=1)
+    else:
+        den = p.sum(axis=1)
+        if correct:
+            top = p.max(axis=1)
+            den = den + (_bf16(top) - top)
+    return _bf16(num / den[:, None])
+
+
+def _dominated_rows(rng, n=4000, keys=128, d=64):
+    x = rng.normal(0.0, 1.0, size=(n, keys)) - 30.0          # other keys far below ...
+    x[:, 0] = rng.uniform(-0.5, 0.5, size=n)                  # ... one key near the reference max
+    v = _bf16(rng.uniform(4.0, 7.99, size=(keys, d)) * rng.choice([-1.0, 1.0], size=(keys, d)))
+    return x, v
+
+
+def test_correction_makes_dominated_rows_exact_up_to_output_rounding():
+    rng = np.random.default_rng(5)
+    x, v = _dominated_rows(rng)
+    w = np.exp2(x - x.max(axis=1, keepdims=True))
+    exact = (w / w.sum(axis=1, keepdims=True)) @ v
+    err_plain = np.abs(_model(x, v, correct=False) - exact).max()
+    err_fixed = np.abs(_model(x, v, correct=True) - exact).max()
+    err_full = np.abs(_model(x, v, correct=False, full=True) - exact).max()
+    half_step = 2.0 ** -6  # half a bf16 step for |O| in [4, 8)
+    assert err_plain > 2e-2, f"uncorrected sum: {err_plain:.4g} (the mismatch should show)"
+    assert err_fixed <= half_step * 1.001, f"corrected sum: {err_fixed:.4g}"
+    assert err_full <= half_step * 1.001, f"rounded sum: {err_full:.4g}"
+
+
+def test_correction_is_harmless_on_flat_rows():
+    rng = np.random.default_rng(6)
+    x = rng.normal(0.0, 1.0, size=(2000, 128))
+    x -= x.max(axis=1, keepdims=True)
+    v = _bf16(rng.normal(0.0, 1.0, size=(128, 64)))
+    w = np.exp2(x)
+    exact = (w / w.sum(axis=1, keepdims=True)) @ v
+    for correct in (False, True):
+        assert np.abs(_model(x, v, correct=correct) - exact).max() < 5e-3
