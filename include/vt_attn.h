@@ -19,7 +19,9 @@
  * of the current device).
  *
  * Element types.  VT_BF16: bf16 in, bf16 out, products accumulated in fp32 on the
- * tensor cores (probabilities are rounded to bf16 before the P*V product).
+ * tensor cores (probabilities are rounded to bf16 before the P*V product; the row sum
+ * that normalises O counts each key tile's largest probability at its bf16 value, so a
+ * row dominated by one key reproduces that key's value row).
  * VT_F32: fp32 in, fp32 out, products on the TF32 tensor-core path with fp32
  * accumulation (inputs and probabilities keep the TF32 subset of their bits).
  *
