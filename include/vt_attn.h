@@ -21,7 +21,11 @@
  * Element types.  VT_BF16: bf16 in, bf16 out, products accumulated in fp32 on the
  * tensor cores (probabilities are rounded to bf16 before the P*V product; the row sum
  * that normalises O counts each key tile's largest probability at its bf16 value, so a
- * row dominated by one key reproduces that key's value row).
+ * row dominated by one key reproduces that key's value row up to the output rounding.
+ * That holds for one dominating key per tile: when two or more keys of a tile carry most
+ * of a row's weight, the bf16 rounding of the others' probabilities stays in the result,
+ * an error of up to about 2^-9 of |O| on top of the output rounding; for |V| in [4, 8)
+ * that is about 0.03).
  * VT_F32: fp32 in, fp32 out, products on the TF32 tensor-core path with fp32
  * accumulation (inputs and probabilities keep the TF32 subset of their bits).
  *
@@ -30,18 +34,21 @@
  *
  * Writes.  Only O's logical elements (i < S_q, e < D_v of each (b, h)) are written;
  * memory between rows or heads of a strided O is never touched.  O must not overlap
- * Q, K or V.
+ * Q, K or V, and no two of O's logical elements may share an address (the strides may
+ * nest the b, h and s indices in any order, e.g. [B,S,H,D], with any padding).
  *
  * Asynchrony.  Calls enqueue work on `stream` and return without waiting.  A kernel
  * that detects a problem on the device (a pipeline wait that exceeds its time limit)
- * records it in a device status word instead of faulting; vt_last_device_status
- * synchronises the stream and returns (and clears) that status.  If the environment
- * variable VT_CHECK is set to a non-zero value, every call does this itself.
+ * records it in the device status word of the stream it was launched on instead of
+ * faulting; vt_last_device_status(stream) synchronises that stream and returns (and
+ * clears) that stream's status only.  If the environment variable VT_CHECK is set to a
+ * non-zero value, every call does this itself.
  *
  * Argument errors are detected on the host before anything is launched:
  *   VT_ERR_INVALID_ARG   a NULL pointer, a negative extent, S_k, D_qk or D_v equal to 0,
- *                        an unknown dtype, a non-finite scale, O overlapping Q/K/V,
- *                        or a non-positive stride;
+ *                        an unknown dtype, a non-finite scale, O overlapping Q/K/V or
+ *                        itself, a non-positive stride, or (vt_attn_fwd) extents whose
+ *                        packed element count overflows 64 bits;
  *   VT_ERR_UNSUPPORTED   D_qk or D_v above 128, S_q or S_k above 2^30, B or H above
  *                        2^31 - 1, a (b, h, s) stride of 2^40 bytes or more (beyond a TMA
  *                        tensor map), or more than 2^31 - 1 work units (query blocks x heads x
@@ -268,9 +275,16 @@ vt_status vt_attn_fwd_general(const void *Q, const int64_t q_stride[3],
 const char *vt_status_str(vt_status status);
 
 /*
- * Synchronise `stream`, then return and clear the device status word of the current
- * device: VT_OK, VT_ERR_DEVICE_TIMEOUT or VT_ERR_DEVICE_BOUNDS; VT_ERR_CUDA if the
- * synchronisation itself reports an error.
+ * Synchronise `stream`, then return and clear the device status word that the kernels launched on
+ * `stream` (on the current device) write: VT_OK, VT_ERR_DEVICE_TIMEOUT or VT_ERR_DEVICE_BOUNDS;
+ * VT_ERR_CUDA if the synchronisation itself reports an error.  Other streams' words are neither read
+ * nor cleared, and no other stream is waited for.
+ *
+ * Words are kept per stream handle: the first 255 distinct handles a process passes to this library get
+ * a word each, in order of first use, and any later handle shares one common word (a destroyed stream's
+ * handle keeps its word, which a new stream that receives the same handle inherits).  The per-thread
+ * default stream is one handle for all threads.  A launch captured into a CUDA graph writes the word of
+ * the stream it was captured on, whichever stream the graph is later launched into.
  */
 vt_status vt_last_device_status(vt_stream_t stream);
 

@@ -21,7 +21,11 @@
 
 namespace vt {
 
-__device__ unsigned g_status_word;  // device status bits (kStatusTimeout, kStatusBounds)
+// Device status words (kStatusTimeout, kStatusBounds), one per stream slot: a launch records what its
+// kernels detect in the slot of the stream it was issued on, and vt_last_device_status reads only that
+// stream's slot.  Slot 0 is shared by the streams beyond the table (kStatusSlots - 1 distinct streams).
+constexpr int kStatusSlots = 256;
+__device__ unsigned g_status[kStatusSlots];
 
 // Work-unit counters of the persistent bf16 kernel: two words per slot, zero between launches (the
 // last CTA of a launch resets its slot).  Static, so no call allocates.
@@ -94,14 +98,14 @@ bool env_check() {
     return on;
 }
 
-// Per-device facts that do not change while the process runs, looked up once: the SM count, the
-// device address of the status word, and the dynamic shared memory already granted per kernel.
+// Per-device facts that do not change while the process runs, looked up once: the SM count, the L2
+// size and the device addresses of the status words and the work-unit counters.
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     long long l2_bytes = 0;
-    unsigned *status = nullptr;
-    unsigned *sched = nullptr;  // g_sched on this device
+    unsigned *status = nullptr;  // g_status on this device
+    unsigned *sched = nullptr;   // g_sched on this device
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_info_mu;
@@ -124,7 +128,7 @@ bool device_info(int dev, DeviceInfo *out) {
         int l2 = 0;
         if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return false;
         d.l2_bytes = l2;
-        if (cudaGetSymbolAddress(&status_ptr, g_status_word) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(&status_ptr, g_status) != cudaSuccess) return false;
         if (cudaGetSymbolAddress(&sched_ptr, g_sched) != cudaSuccess) return false;
         d.status = static_cast<unsigned *>(status_ptr);
         d.sched = static_cast<unsigned *>(sched_ptr);
@@ -132,6 +136,22 @@ bool device_info(int dev, DeviceInfo *out) {
     }
     *out = d;
     return true;
+}
+
+// The status slot of a stream: the first kStatusSlots - 1 distinct stream handles seen get slots 1, 2, ...
+// in order of first use; later ones share slot 0.  Handles are process-wide, so one table serves every
+// device (each device has its own array of words).
+std::mutex g_slot_mu;
+cudaStream_t g_slot_stream[kStatusSlots];
+int g_n_slots = 1;
+
+int status_slot(cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_slot_mu);
+    for (int i = 1; i < g_n_slots; ++i)
+        if (g_slot_stream[i] == s) return i;
+    if (g_n_slots == kStatusSlots) return 0;
+    g_slot_stream[g_n_slots] = s;
+    return g_n_slots++;
 }
 
 // cudaFuncSetAttribute for the dynamic shared memory size, only when a kernel needs more on a
@@ -313,7 +333,7 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
     int dev = 0;
     DeviceInfo info;
     if (cudaGetDevice(&dev) != cudaSuccess || !device_info(dev, &info)) return VT_ERR_CUDA;
-    p.status = info.status;
+    p.status = info.status + status_slot(stream);
     const int sms = info.sms;
 
     if constexpr (DT == kBF16) {
@@ -397,14 +417,17 @@ void *noalloc_scratch(int dev) {
     return addr[dev];
 }
 
+// Wait for `stream`, then read and clear the status word of its slot on the current device.  The read and
+// the clear are ordered on `stream` itself, so no other stream is waited for.
 vt_status read_status(cudaStream_t stream) {
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return VT_ERR_CUDA;
+    int dev = 0;
+    DeviceInfo info;
+    if (cudaGetDevice(&dev) != cudaSuccess || !device_info(dev, &info)) return VT_ERR_CUDA;
+    unsigned *word = info.status + status_slot(stream);
     unsigned w = 0;
-    if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof w) != cudaSuccess) return VT_ERR_CUDA;
-    if (w) {
-        const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return VT_ERR_CUDA;
-    }
+    if (cudaMemcpyAsync(&w, word, sizeof w, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return VT_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return VT_ERR_CUDA;
+    if (w && cudaMemsetAsync(word, 0, sizeof w, stream) != cudaSuccess) return VT_ERR_CUDA;
     if (w & kStatusTimeout) return VT_ERR_DEVICE_TIMEOUT;
     if (w & kStatusBounds) return VT_ERR_DEVICE_BOUNDS;
     return VT_OK;
@@ -438,9 +461,9 @@ vt_status vt_last_device_status(vt_stream_t stream) {
 namespace vt {
 namespace {
 
-// Argument checks shared by every forward entry point (see include/vt_attn.h); VT_OK with
-// *empty = true for a valid empty problem.
-vt_status check_args(const Problem &P, bool *empty) {
+// The checks of include/vt_attn.h that need only the extents and scalars (in the header's order of
+// precedence); VT_OK with *empty = true for a valid empty problem.
+vt_status check_shape(const Problem &P, bool *empty) {
     *empty = false;
     const int64_t B = P.B, H = P.H, H_kv = P.H_kv, S_q = P.S_q, S_k = P.S_k, D_qk = P.D_qk, D_v = P.D_v;
     if (P.dtype != VT_F32 && P.dtype != VT_BF16) return VT_ERR_INVALID_ARG;
@@ -455,10 +478,36 @@ vt_status check_args(const Problem &P, bool *empty) {
     if (D_qk > vt::kMaxD || D_v > vt::kMaxD) return VT_ERR_UNSUPPORTED;
     if (B > vt::kMaxExtent || H > vt::kMaxExtent || S_q > vt::kMaxSeq || S_k > vt::kMaxSeq)
         return VT_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || S_q == 0) {
-        *empty = true;
-        return VT_OK;
+    if (B == 0 || H == 0 || S_q == 0) *empty = true;
+    return VT_OK;
+}
+
+// True when no two logical elements of a [B, H, S, D] tensor with (b, h, s) strides st and unit stride
+// along D share an address: with the extents of size 1 left out and the rest taken in order of
+// increasing stride, each stride reaches past everything the smaller ones span.  This accepts every
+// nesting of the three indices ([B,H,S,D], [B,S,H,D], ...) without gaps or overlap, and any padding.
+bool rows_disjoint(const int64_t st[3], int64_t B, int64_t H, int64_t S, int64_t D) {
+    int64_t n[3] = {B, H, S}, s[3] = {st[0], st[1], st[2]};
+    for (int i = 0; i < 3; ++i)  // insertion sort by stride
+        for (int j = i; j > 0 && s[j] < s[j - 1]; --j) {
+            const int64_t ts = s[j], tn = n[j];
+            s[j] = s[j - 1]; n[j] = n[j - 1];
+            s[j - 1] = ts; n[j - 1] = tn;
+        }
+    int64_t span = D;  // elements covered by the dimensions taken so far, as one contiguous extent
+    for (int i = 0; i < 3; ++i) {
+        if (n[i] <= 1) continue;
+        if (s[i] < span) return false;
+        int64_t t = 0;
+        if (__builtin_mul_overflow(n[i] - 1, s[i], &t) || __builtin_add_overflow(span, t, &span)) return false;
     }
+    return true;
+}
+
+// The checks of include/vt_attn.h on pointers, strides and the memory they describe (after check_shape
+// passed on a non-empty problem).
+vt_status check_memory(const Problem &P) {
+    const int64_t B = P.B, H = P.H, H_kv = P.H_kv, S_q = P.S_q, S_k = P.S_k, D_qk = P.D_qk, D_v = P.D_v;
     if (!P.Q || !P.K || !P.V || !P.O || !P.qs || !P.ks || !P.vs || !P.os) return VT_ERR_INVALID_ARG;
     const int elt = P.dtype == VT_BF16 ? 2 : 4;
     const int64_t *st[4] = {P.qs, P.ks, P.vs, P.os};
@@ -479,6 +528,8 @@ vt_status check_args(const Problem &P, bool *empty) {
         !vt::span_of(P.V, P.vs, B, H_kv, S_k, D_v, elt, &sv) || !vt::span_of(P.O, P.os, B, H, S_q, D_v, elt, &so))
         return VT_ERR_INVALID_ARG;
     if (vt::overlap(so, sq) || vt::overlap(so, sk) || vt::overlap(so, sv)) return VT_ERR_INVALID_ARG;
+    // every output element has an address of its own (several CTAs would otherwise race on one)
+    if (!vt::rows_disjoint(P.os, B, H, S_q, D_v)) return VT_ERR_INVALID_ARG;
     if (P.lse) {
         if (reinterpret_cast<uintptr_t>(P.lse) % 4) return VT_ERR_INVALID_ARG;
         vt::Span sl;
@@ -487,6 +538,14 @@ vt_status check_args(const Problem &P, bool *empty) {
             return VT_ERR_INVALID_ARG;
     }
     return VT_OK;
+}
+
+// Every argument check shared by the forward entry points; VT_OK with *empty = true for a valid empty
+// problem.
+vt_status check_args(const Problem &P, bool *empty) {
+    const vt_status r = check_shape(P, empty);
+    if (r != VT_OK || *empty) return r;
+    return check_memory(P);
 }
 
 // Checks of a split-KV workspace (n_split > 1): present, large enough, 256-byte aligned and clear of
@@ -668,10 +727,21 @@ vt_status vt_attn_fwd(const void *Q, const void *K, const void *V, void *O, int6
                       int64_t S_k, int64_t D_qk, int64_t D_v, float scale, int causal, vt_dtype dtype,
                       vt_stream_t stream) {
     const vt::NvtxRange range("vt_attn_fwd");
-    const int64_t qs[3] = {H * S_q * D_qk, S_q * D_qk, D_qk};
-    const int64_t ks[3] = {H * S_k * D_qk, S_k * D_qk, D_qk};
-    const int64_t vs[3] = {H * S_k * D_v, S_k * D_v, D_v};
-    const int64_t os[3] = {H * S_q * D_v, S_q * D_v, D_v};
+    // Packed strides, formed only from extents that passed the shape checks and only when the products
+    // fit in 64 bits: a packed tensor whose element count overflows cannot exist.
+    const int64_t unit[3] = {1, 1, 1};
+    vt::Problem P = vt::plain_problem(Q, unit, K, unit, V, unit, O, unit, B, H, S_q, S_k, D_qk, D_v, scale, causal,
+                                      dtype);
+    bool empty = false;
+    const vt_status c = vt::check_shape(P, &empty);
+    if (c != VT_OK || empty) return c;
+    auto packed = [](int64_t H_, int64_t S, int64_t D, int64_t out[3]) {
+        out[2] = D;
+        return !__builtin_mul_overflow(S, D, &out[1]) && !__builtin_mul_overflow(H_, out[1], &out[0]);
+    };
+    int64_t qs[3], ks[3], vs[3], os[3];
+    if (!packed(H, S_q, D_qk, qs) || !packed(H, S_k, D_qk, ks) || !packed(H, S_k, D_v, vs) || !packed(H, S_q, D_v, os))
+        return VT_ERR_INVALID_ARG;
     return vt_attn_fwd_ex(Q, qs, K, ks, V, vs, O, os, B, H, S_q, S_k, D_qk, D_v, scale, causal, dtype, nullptr,
                           stream);
 }

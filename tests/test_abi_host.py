@@ -195,3 +195,44 @@ def test_general_empty_problem_and_null_mask(lib):
     assert general_call(n_split=2, ws=8 * A, ws_bytes=1 << 24, dtype=vt.VT_F32) == 4
     assert split_call(dtype=vt.VT_F32) == 4
     assert vt.vt_last_device_status(0) == 4
+
+
+# ---------------------------------------------------------------- extents whose packed size overflows
+
+def test_packed_strides_that_overflow_are_rejected(lib):
+    # every extent is within the limits, but H * S * D of the packed layout does not fit in 64 bits
+    H, S = (1 << 31) - 1, 1 << 30
+    assert vt.vt_attn_fwd(A, 2 * A, 3 * A, 4 * A, 1, H, S, S, 128, 128, 0.5, 0, vt.VT_BF16, None) == 1
+    assert vt.vt_attn_fwd(A, 2 * A, 3 * A, 4 * A, 1, H, S, S, 128, 128, 0.5, 1, vt.VT_F32, None) == 1
+    # shape errors keep their own codes and precedence
+    assert vt.vt_attn_fwd(A, 2 * A, 3 * A, 4 * A, 1, H, S, S, 129, 128, 0.5, 0, vt.VT_BF16, None) == 2
+    assert vt.vt_attn_fwd(A, 2 * A, 3 * A, 4 * A, -1, H, S, S, 128, 128, 0.5, 0, vt.VT_BF16, None) == 1
+    assert vt.vt_attn_fwd(A, 2 * A, 3 * A, 4 * A, 0, H, S, S, 128, 128, 0.5, 0, vt.VT_BF16, None) == 0
+
+
+# ---------------------------------------------------------------- output elements must not share addresses
+
+@pytest.mark.parametrize("o_stride,H,S_q,dtype", [
+    ((64, 64, 4), 1, 4, vt.VT_F32),    # rows 4 elements apart, 8 wide
+    ((256, 8, 8), 2, 4, vt.VT_BF16),   # heads and rows on the same stride
+    ((16, 64, 8), 2, 4, vt.VT_BF16),   # batches 16 elements apart, inside the 32 elements of a head's rows
+])
+def test_self_overlapping_output_is_rejected(lib, o_stride, H, S_q, dtype):
+    B = 2
+    sq = (H * S_q * 8, S_q * 8, 8)
+    skv = (H * 4 * 8, 4 * 8, 8)
+    assert vt.vt_attn_fwd_strided(A, sq, 2 * A, skv, 3 * A, skv, 8 * A, o_stride, B, H, S_q, 4, 8, 8, 0.5, 0,
+                                  dtype, None) == 1
+
+
+def test_other_output_nestings_pass_the_checks(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: a valid call would launch on these fake addresses")
+    # [B, S, H, D] output (heads interleaved within each row block) and a padded one reach the launch
+    B, H, S_q, D = 2, 2, 4, 8
+    sq = (H * S_q * D, S_q * D, D)
+    skv = (H * 4 * D, 4 * D, D)
+    for o_stride in ((S_q * H * D, D, H * D), (H * S_q * 24, S_q * 24, 24)):
+        assert vt.vt_attn_fwd_strided(A, sq, 2 * A, skv, 3 * A, skv, 8 * A, o_stride, B, H, S_q, 4, D, D, 0.5, 0,
+                                      vt.VT_BF16, None) == 4

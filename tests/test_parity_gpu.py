@@ -241,6 +241,23 @@ def test_stalled_pipeline_reports_timeout_and_context_survives():
     check(got, oracle.attn_fwd(q, k, v, 0.125, False), "bf16", "after timeout")
 
 
+def test_device_status_is_kept_per_stream():
+    """A time-out on one stream is reported to that stream only: a caller polling another stream sees VT_OK
+    and does not clear it.  Both element types' kernels, each on its own pair of streams."""
+    for dtype, seed in (("bf16", 17), ("f32", 18)):
+        q, k, v = synth.make_qkv(1, 2, 256, 256, 64, 64, dtype, seed=seed)
+        Q, K, V = to_device(q), to_device(k), to_device(v)
+        stalled, healthy = torch.cuda.Stream(), torch.cuda.Stream()
+        opts = vt.vt_attn_opts(wait_timeout_ns=20_000_000, flags=vt.VT_OPT_TEST_STALL)
+        vt.attn_fwd(Q, K, V, scale=0.125, opts=opts, stream=stalled)
+        out = vt.attn_fwd(Q, K, V, scale=0.125, stream=healthy)
+        assert vt.vt_last_device_status(healthy) == 0
+        assert vt.vt_last_device_status(stalled) == 5  # still there after the other stream's poll
+        assert vt.vt_last_device_status(stalled) == 0  # cleared by its own poll
+        healthy.synchronize()
+        check(to_host64(out), oracle.attn_fwd(q, k, v, 0.125, False), dtype, f"{dtype} beside a stalled stream")
+
+
 def test_rows_dominated_by_one_key_reproduce_its_value_row():
     """Where one key carries all but ~1e-4 of a row's weight, the output must round to that key's V values:
     P V multiplies the dominant P rounded to bf16, and the row sum has to weigh it the same way (a mismatch

@@ -4,8 +4,9 @@ Some callers may not call cudaMalloc at all: a plugin inside a host framework th
 of device memory, or a latency-critical service that must not allocate after start-up because an
 allocation can block and synchronise the device.  This entry point keeps the shares' partial
 results in the library's fixed 32 MiB device array instead of a caller workspace.  The GPU test
-checks it against the workspace-taking entry point on two calls in a row (the second call finds
-the first call's data still in the shared array); the host tests check the size limit.
+checks it against the workspace-taking entry point and against the fp64 oracle on calls in a row
+(each later call finds the earlier calls' data still in the shared array), for both element types;
+the host tests check the size limit.
 """
 
 from __future__ import annotations
@@ -15,6 +16,7 @@ import math
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from gpu_util import check, to_device, to_host64
 
@@ -49,20 +51,24 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     vt.load()
     stream = torch.cuda.current_stream().cuda_stream
     calls = [
-        # B, H, S_q, S_k, D_qk, D_v, causal, n_split
-        (1, 4, 200, 4096, 128, 128, False, 6),
-        (2, 2, 64, 3000, 64, 64, True, 4),
+        # B, H, S_q, S_k, D_qk, D_v, causal, n_split, dtype
+        (1, 4, 200, 4096, 128, 128, False, 6, "bf16"),
+        (2, 2, 64, 3000, 64, 64, True, 4, "bf16"),
+        (1, 2, 100, 2000, 72, 72, False, 3, "f32"),
     ]
-    for i, (B, H, S_q, S_k, D_qk, D_v, causal, n_split) in enumerate(calls):
+    for i, (B, H, S_q, S_k, D_qk, D_v, causal, n_split, dtype) in enumerate(calls):
         assert vt.vt_attn_splitkv_workspace_size(B, H, S_q, D_v, n_split) <= LIMIT
-        q, k, v = synth.make_qkv(B, H, S_q, S_k, D_qk, D_v, "bf16", seed=50 + i)
+        q, k, v = synth.make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype, seed=50 + i)
         scale = float(np.float32(1.0 / math.sqrt(D_qk)))
         Q, K, V = to_device(q), to_device(k), to_device(v)
         O_ref = vt.attn_fwd_splitkv(Q, K, V, scale=scale, causal=causal, n_split=n_split)
         O = torch.empty_like(O_ref)
+        code = vt.VT_BF16 if dtype == "bf16" else vt.VT_F32
         rc = vt.vt_attn_fwd_splitkv_noalloc(Q.data_ptr(), _strides(Q), K.data_ptr(), _strides(K), V.data_ptr(),
                                             _strides(V), O.data_ptr(), _strides(O), B, H, S_q, S_k, D_qk, D_v,
-                                            scale, causal, vt.VT_BF16, n_split, stream)
+                                            scale, causal, code, n_split, stream)
         assert rc == 0
         assert vt.vt_last_device_status(stream) == 0
-        check(to_host64(O), to_host64(O_ref), "bf16", f"no-alloc call {i + 1}")
+        got = to_host64(O)
+        check(got, to_host64(O_ref), dtype, f"no-alloc call {i + 1} vs the workspace entry point")
+        check(got, oracle.attn_fwd(q, k, v, scale, causal), dtype, f"no-alloc call {i + 1} vs the oracle")
