@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libvt_attn.so")
 LIB_DEBUG = os.path.join(PKG, "libvt_attn_debug.so")
 SOURCES = [os.path.join(CSRC, "vt_attn_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vt_attn_kernel.cuh", "vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_attn_merge.cuh",
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("vt_attn_f32_2q.cuh", "vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_attn_merge.cuh",
                                                   "vt_ptx.cuh")] + [
     os.path.join(os.path.dirname(PKG), "include", "vt_attn.h")]
 

@@ -16,7 +16,7 @@
 
 #include "../../include/vt_attn.h"
 #include "vt_attn_bf16_2q.cuh"
-#include "vt_attn_kernel.cuh"
+#include "vt_attn_f32_2q.cuh"
 #include "vt_attn_merge.cuh"
 
 namespace vt {
@@ -275,9 +275,26 @@ vt_status merge(const AttnParams &p, const Problem &P, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? VT_OK : VT_ERR_CUDA;
 }
 
+// Per element type: bytes per element, keys per K/V tile and the MMA K-step (bf16 16, tf32 8).
+template <int DT>
+struct Elt {
+    static constexpr int kElt = DT == kBF16 ? 2 : 4;
+    static constexpr int kBN = DT == kBF16 ? q2::kBN : f2::kBN;
+    static constexpr int kKStep = DT == kBF16 ? 16 : 8;
+    static constexpr int kChunkElems = 128 / kElt;  // elements per 128-byte chunk
+};
+
+// A cluster size for the fp32 kernel: the most CTAs (8, 4 or 2) that may share one unit's key tiles while
+// every CTA of the launch still fits one wave and keeps two key tiles or more; 1 when that does not pay.
+int f32_cluster_size(long long units, long long key_tiles, int sms) {
+    for (int c = f2::kMaxCluster; c >= 2; c /= 2)
+        if (units * c <= sms && key_tiles >= 2LL * c) return c;
+    return 1;
+}
+
 template <int DT>
 vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *workspace, cudaStream_t stream) {
-    using C = Cfg<DT>;
+    using C = Elt<DT>;
     const void *Q = P.Q, *K = P.K, *V = P.V;
     void *O = P.O;
     const int64_t *qs = P.qs, *ks = P.ks, *vs = P.vs, *os = P.os;
@@ -288,11 +305,8 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
     if (!make_map(&tq, Q, qs, B, H, S_q, D_qk, C::kElt, kBM) ||
         !make_map(&tk, K, ks, B, P.H_kv, S_k, D_qk, C::kElt, kv_rows))
         return VT_ERR_CUDA;
-    if (DT == kBF16) {
-        if (!make_map(&tv, V, vs, B, P.H_kv, S_k, D_v, C::kElt, kv_rows)) return VT_ERR_CUDA;
-    } else {
-        tv = tk;  // fp32: V is read by the kernel's transposing loader warps, not by TMA
-    }
+    // (fp32: Q is read by the kernel's softmax threads, which write it into TMEM)
+    if (!make_map(&tv, V, vs, B, P.H_kv, S_k, D_v, C::kElt, kv_rows)) return VT_ERR_CUDA;
 
     AttnParams p{};
     p.B = static_cast<int>(B);
@@ -318,6 +332,12 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
     p.v_sb = vs[0];
     p.v_sh = vs[1];
     p.v_ss = vs[2];
+    p.Q = Q;
+    p.q_sb = qs[0];
+    p.q_sh = qs[1];
+    p.q_ss = qs[2];
+    p.tiles_per_unit = 2;
+    p.cluster = 1;
     p.n_split = n_split;
     if (n_split > 1) {
         const SplitLayout L = split_layout(B, H, S_q, D_v, n_split);
@@ -376,26 +396,55 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         if (n_split > 1) return merge<2>(p, P, stream);
         return VT_OK;
     } else {
-        // one 128-row query tile per CTA (fp32 I/O on the TF32 path)
-        const int q_bytes = p.q_chunks * kBM * 128;
-        const int kv_bytes = p.q_chunks * C::kBN * 128 + v_stage_bytes<DT>(p.v_chunks, p.n_pv);
-        const int budget = kSmemLimit - 1024 /*alignment slack*/ - static_cast<int>(sizeof(SharedCtl)) - 256;
-        p.stages = (budget - q_bytes) / kv_bytes;
-        if (p.stages > kMaxStages) p.stages = kMaxStages;
-        if (p.stages < 2) return VT_ERR_UNSUPPORTED;
-        const int smem = 1024 + q_bytes + p.stages * kv_bytes;
-        p.head_group = 1;
-        // Q K^T K-steps of 8 tf32, rounded up to whole 128-byte chunks (the TMA zero-fills past D_qk)
-        const int chunks = p.q_chunks;
+        // fp32 I/O on the TF32 path: units of two 128-row query tiles when TMEM holds both tiles' S, O and Q
+        // (D_qk rounded up to 8 plus D_v rounded up to 16 at most 192), else one; one CTA per unit and share.
+        const int dq = p.qk_ksteps * 8;
+        const int stage_bytes = (p.q_chunks + p.v_chunks) * f2::kBN * 128 + p.n_pv * f2::kBN * 4;
+        const int budget = kSmemLimit - 1024 - static_cast<int>(sizeof(f2::Ctl)) - 256;
+        p.stages = budget / stage_bytes;
+        if (p.stages > f2::kMaxStages) p.stages = f2::kMaxStages;
+        // The Q tiles arrive in the last stages' memory, and at least one stage must stay outside it: two tiles
+        // when that fits and TMEM holds both tiles' S, O and Q, else one.
+        auto q_stages = [&](int tiles) { return (tiles * p.q_chunks * kBM * 128 + stage_bytes - 1) / stage_bytes; };
+        int T = 2 * (f2::kBN + p.n_pv + dq) <= 512 && p.stages >= q_stages(2) + 1 ? 2 : 1;
+        if (p.stages < 2 || p.stages < q_stages(T) + 1) return VT_ERR_UNSUPPORTED;
+        p.tiles_per_unit = T;
+        p.n_qblocks = static_cast<int>((S_q + kBM * T - 1) / (kBM * T));
+        const long long units = static_cast<long long>(p.n_qblocks) * B * H;
+        // Without a caller's split, a unit's key tiles may be shared by the CTAs of a cluster, which merge
+        // their results in distributed shared memory; the partials each CTA receives reuse its K/V ring.
+        int cl = 1;
+        if (n_split == 1) {
+            const long long key_tiles = (S_k + f2::kBN - 1) / f2::kBN;
+            cl = f32_cluster_size(units, key_tiles, sms);
+            while (cl > 4 * T) cl /= 2;  // each CTA owns whole warps of rows (T * 128 / cl >= 32) in the merge
+            // the merge stages every row of the unit and receives the other CTAs' rows in the ring's memory
+            const long long merge_bytes = 2LL * T * kBM * ((D_v + 3) / 4 + 1) * 16;
+            if (merge_bytes > static_cast<long long>(p.stages) * stage_bytes) cl = 1;
+        }
+        p.cluster = cl;
+        const long long ctas = units * (cl > 1 ? cl : n_split);
+        if (ctas > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
+        p.n_units = static_cast<int>(units);
+        const int smem = 1024 + p.stages * stage_bytes;
         void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
-            chunks <= 1 ? attn_fwd_kernel<DT, 4>
-                        : chunks == 2 ? attn_fwd_kernel<DT, 8>
-                                      : chunks == 3 ? attn_fwd_kernel<DT, 12> : attn_fwd_kernel<DT, 16>;
+            dq <= 32 ? attn_fwd_f32_2q_kernel<4>
+                     : dq <= 64 ? attn_fwd_f32_2q_kernel<8>
+                                : dq <= 96 ? attn_fwd_f32_2q_kernel<12> : attn_fwd_f32_2q_kernel<16>;
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
-        const long long items = static_cast<long long>(p.n_qblocks) * B * H * n_split;
-        if (items > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
-        p.n_units = static_cast<int>(items);
-        kern<<<static_cast<unsigned>(items), C::kThreads, smem, stream>>>(tq, tk, tv, p);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+        cfg.blockDim = dim3(f2::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = cl > 1 ? 1 : 0;
+        if (cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p) != cudaSuccess) return VT_ERR_CUDA;
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;
         if (n_split > 1) return merge<4>(p, P, stream);
         return VT_OK;
@@ -650,14 +699,16 @@ size_t vt_attn_splitkv_workspace_size(int64_t B, int64_t H, int64_t S_q, int64_t
 int vt_attn_splitkv_choose(int64_t B, int64_t H, int64_t S_q, int64_t S_k, int causal, vt_dtype dtype) {
     (void)causal;
     if ((dtype != VT_BF16 && dtype != VT_F32) || B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return 1;
+    // fp32: the plain call already spreads a unit's key tiles over the CTAs of a cluster
+    if (dtype == VT_F32) return 1;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
     // Shares only pay when every CTA still fits in one wave, and each share keeps >= 4 key tiles.
     // work items and key tiles of the kernel that serves the dtype
-    const long long rows = dtype == VT_BF16 ? vt::q2::kRows : vt::kBM;
-    const long long bn = dtype == VT_BF16 ? vt::q2::kBN : vt::Cfg<vt::kF32>::kBN;
+    const long long rows = vt::q2::kRows;
+    const long long bn = vt::q2::kBN;
     const long long items = B * H * ((S_q + rows - 1) / rows);
     const long long tiles = (S_k + bn - 1) / bn;
     long long n = items >= sms ? 1 : sms / items;

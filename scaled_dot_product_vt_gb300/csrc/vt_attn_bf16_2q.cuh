@@ -89,12 +89,6 @@ struct Ctl {
     volatile uint32_t abort_flag;
 };
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 
 // Units run over groups of `head_group` heads; inside a group, the heaviest query blocks first
 // when work grows with the block index; the shares of one block are adjacent.

@@ -10,9 +10,7 @@
 namespace vt {
 
 constexpr int kBM = 128;           // query rows per work item (= TMEM lanes)
-constexpr int kMaxStages = 4;
 constexpr int kMaxSplit = 64;       // split-KV shares per work item, at most
-constexpr float kRescaleTau = 8.0f;  // log2 units: rescale O only when the row max grows by more
 
 constexpr long long kBandInf = 1LL << 42;  // a band edge that no row reaches
 
@@ -43,6 +41,12 @@ struct AttnParams {
     long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
     const void *V;               // read by the fp32 V loader
     long long v_sb, v_sh, v_ss;
+    const void *Q;               // read by the fp32 kernel's softmax threads (Q goes to TMEM)
+    long long q_sb, q_sh, q_ss;
+    // fp32 kernel: query tiles per work unit (1 or 2), and the CTAs of a thread-block cluster that share
+    // one unit's key tiles and merge their results in distributed shared memory (1: no cluster)
+    int tiles_per_unit;
+    int cluster;
     // Split-KV: each work item's key tiles are cut into n_split contiguous ranges, one per CTA; with
     // n_split > 1 the CTAs write unnormalised partial outputs (fp32, D_v per row), their row max m
     // (log2 units, -inf if no allowed key), row sum l and the correction that makes l + corr weigh P
@@ -129,6 +133,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0) {
+            if (abort_flag) return false;
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                abort_flag = 1;
+                atomicOr(p.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait until a shared-memory counter exceeds `above`, with the same time limit and abort shortcut as
+// wait_bounded.
+__device__ __forceinline__ bool wait_flag_above(volatile uint32_t &flag, int above, volatile uint32_t &abort_flag,
+                                                const AttnParams &p) {
+    if (static_cast<int>(flag) > above) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (static_cast<int>(flag) > above) return true;
         if ((n & 63u) == 0) {
             if (abort_flag) return false;
             if (globaltimer_ns() - t0 > p.timeout_ns) {
