@@ -53,8 +53,11 @@ DEFAULT_WORKLOAD = "bf16_causal_8k_peaky"
 KERNEL_SOURCES = [os.path.join(ROOT, "scaled_dot_product_vt_gb300", "csrc", f)
                   for f in ("vt_attn_bf16_2q.cuh", "vt_attn_common.cuh", "vt_ptx.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
-# nominal dense tf32 : bf16 tensor ratio (1.1 : 2.25 PFLOP/s), applied to the measured bf16 peak
+# nominal dense tf32 : bf16 tensor ratio (1.1 : 2.25 PFLOP/s), applied to the measured bf16 peak; the issue-rate
+# probe of tcgen05.mma measured kind::tf32 at exactly half of kind::f16 per clock (4096 vs 8192 flop/clk/SM at
+# every N), which the line reports beside it as peak_probe_ratio
 TF32_OVER_BF16 = 1.1 / 2.25
+TF32_OVER_BF16_PROBE = 0.5
 
 
 def kernel_source_hash() -> str:
@@ -484,7 +487,8 @@ def main() -> int:
                          "frac": achieved / peak, "traffic": load_traffic(w.name),
                          "peak_source": (f"{peaks['source']} bf16 burst" if w.dtype == "bf16"
                                          else f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio"),
-                         "kernel": "vt::attn_fwd_bf16_2q_kernel" if w.dtype == "bf16" else "vt::attn_fwd_kernel<0>",
+                         "kernel": "vt::attn_fwd_bf16_2q_kernel" if w.dtype == "bf16" else "vt::attn_fwd_f32_2q_kernel",
+                         "peak_probe_ratio": None if w.dtype == "bf16" else peaks["bf16"] * TF32_OVER_BF16_PROBE,
                          "launch_ms": per_launch_ms,  # one call: the attention kernel (+ the merge if split)
                          "merge_kernel": "vt::attn_merge_kernel" if n_split > 1 else None},
             "cpu_baseline": cpu,

@@ -8,7 +8,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -26,10 +25,6 @@ namespace vt {
 // stream's slot.  Slot 0 is shared by the streams beyond the table (kStatusSlots - 1 distinct streams).
 constexpr int kStatusSlots = 256;
 __device__ unsigned g_status[kStatusSlots];
-
-// Work-unit counters of the persistent bf16 kernel: two words per slot, zero between launches (the
-// last CTA of a launch resets its slot).  Static, so no call allocates.
-__device__ unsigned g_sched[kSchedSlots * 2];
 
 // Scratch of vt_attn_fwd_splitkv_noalloc, for callers that cannot allocate device memory: a
 // fixed array that exists on every GPU that loads this library, for as long as the process runs.
@@ -99,13 +94,12 @@ bool env_check() {
 }
 
 // Per-device facts that do not change while the process runs, looked up once: the SM count, the L2
-// size and the device addresses of the status words and the work-unit counters.
+// size and the device address of the status words.
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     long long l2_bytes = 0;
     unsigned *status = nullptr;  // g_status on this device
-    unsigned *sched = nullptr;   // g_sched on this device
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_info_mu;
@@ -123,15 +117,13 @@ bool device_info(int dev, DeviceInfo *out) {
     std::lock_guard<std::mutex> lock(g_info_mu);
     DeviceInfo &d = g_info[dev];
     if (!d.ready) {
-        void *status_ptr = nullptr, *sched_ptr = nullptr;
+        void *status_ptr = nullptr;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         int l2 = 0;
         if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return false;
         d.l2_bytes = l2;
         if (cudaGetSymbolAddress(&status_ptr, g_status) != cudaSuccess) return false;
-        if (cudaGetSymbolAddress(&sched_ptr, g_sched) != cudaSuccess) return false;
         d.status = static_cast<unsigned *>(status_ptr);
-        d.sched = static_cast<unsigned *>(sched_ptr);
         d.ready = true;
     }
     *out = d;
@@ -380,10 +372,9 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         const long long units = static_cast<long long>(p.n_qblocks) * bh * n_split;
         if (units > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         p.n_units = static_cast<int>(units);
-        static std::atomic<unsigned> launch_seq{0};
-        p.sched = info.sched + 2 * (launch_seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
-        // persistent: one CTA per SM (the shared memory admits one) draws units until none is left
-        const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
+        // one CTA per unit; the shared memory admits one per SM, and a running CTA takes over the units of
+        // the CTAs that have not started (cluster launch control), so about one per SM runs
+        const unsigned grid = static_cast<unsigned>(units);
         // Q K^T K-steps of 16, rounded up to an even count (the TMA zero-fills past D_qk)
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
         void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =

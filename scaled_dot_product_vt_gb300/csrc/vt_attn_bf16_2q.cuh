@@ -2,9 +2,11 @@
 // 128-key K/V tile, one softmax warpgroup per query tile, tcgen05 issued by one warp (one lane
 // elected per instruction).
 //
-// Persistent: one CTA per SM takes work units in launch order from a global counter (the
-// producer warp draws them and passes them to the other roles through a small ring in shared
-// memory), so the heavy units that come first spread over the SMs as they free up.
+// Persistent through cluster launch control: the grid has one CTA per work unit, but a running CTA
+// takes over the units of CTAs that have not started yet (clusterlaunchcontrol.try_cancel), so about
+// one CTA per SM runs and each one works through units in launch order (the producer warp obtains
+// them and passes them to the other roles through a small ring in shared memory); the heavy units that
+// come first spread over the SMs as they free up.  No state is shared between launches.
 // A unit is 256 query rows of one (b, h) slice, as query tiles t = 0, 1 (rows r0 + 128 t ..
 // r0 + 128 t + 127), and one share of their key tiles.  TMEM, barriers and descriptors live
 // for the whole CTA; every barrier's phase is counted across units, so the producer loads the
@@ -82,7 +84,9 @@ struct Ctl {
     uint64_t o_done[2];   // last P V of tile t done
     uint64_t unit_full[kUnitRing];   // ring entry k written by the producer
     uint64_t unit_empty[kUnitRing];  // ring entry k read by every other role
-    Unit unit[kUnitRing];            // decoded units (u = -1 once the counter is exhausted)
+    Unit unit[kUnitRing];            // decoded units (u = -1 once no CTA is left to take over)
+    uint4 clc_resp;                  // response of the last launch-control request
+    uint64_t clc_full;               // that response has landed
     uint64_t drain;
     uint64_t stall;
     uint32_t tmem_base;
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         }
         mbar_init(smem_u32(&ctl.drain), 1);
         mbar_init(smem_u32(&ctl.stall), 1);
+        mbar_init(smem_u32(&ctl.clc_full), 1);
         ctl.abort_flag = 0;
         fence_mbar_init();
     }
@@ -256,6 +261,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             uint32_t empty_phase = 0;  // bit s: parity of the next empty-phase of slot s to wait for
             int loads = 0, q_loads = 0;
             bool ok = true;
+            bool clc_done = false;
+            uint32_t clc_par = 0;
             for (int n = 0; ok; ++n) {
                 // draw the next unit and publish it to the other roles
                 const int k = n % kUnitRing;
@@ -263,8 +270,20 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     ok = wait_bounded(smem_u32(&ctl.unit_empty[k]), ((n / kUnitRing) - 1) & 1, ctl.abort_flag, p);
                     if (!ok) break;
                 }
-                const unsigned drawn = atomicAdd(&p.sched[0], 1u);
-                const int u = drawn < static_cast<unsigned>(p.n_units) ? static_cast<int>(drawn) : -1;
+                // the CTA's own unit first, then those of CTAs whose launch this one cancels
+                int u = -1;
+                if (n == 0) {
+                    u = static_cast<int>(blockIdx.x);
+                } else if (!clc_done) {
+                    mbar_arrive_expect_tx(smem_u32(&ctl.clc_full), 16);
+                    clc_try_cancel(smem_u32(&ctl.clc_resp), smem_u32(&ctl.clc_full));
+                    ok = wait_bounded(smem_u32(&ctl.clc_full), clc_par, ctl.abort_flag, p);
+                    clc_par ^= 1u;
+                    if (!ok) break;
+                    u = clc_cancelled_x(smem_u32(&ctl.clc_resp));
+                    if (u < 0) clc_done = true;  // no further request once one has found no CTA left
+                }
+                if (u >= p.n_units) u = -1;
                 Unit U;
                 if (u >= 0) {
                     U = decode_unit(p, u);
@@ -669,7 +688,6 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0) sched_release(p);
 }
 
 }  // namespace vt

@@ -23,7 +23,7 @@ enum : int { kF32 = 0, kBF16 = 1 };
 struct AttnParams {
     int B, H, S_q, S_k, D_qk, D_v;
     int n_qblocks;    // query blocks per (b, h): ceil(S_q / rows per block)
-    int n_units;      // work units of a persistent launch: query blocks x heads x batches x n_split
+    int n_units;      // work units of a launch: query blocks x heads x batches x n_split
     int head_group;   // heads whose query blocks are interleaved in the launch order
     int qk_ksteps;    // ceil(D_qk / K-step), K-step = 16 (bf16) or 8 (tf32)
     int q_chunks;     // 128-byte column chunks of a Q/K row: ceil(D_qk * elt / 128)
@@ -58,26 +58,8 @@ struct AttnParams {
     float *part_c;
     unsigned long long timeout_ns;
     unsigned flags;
-    unsigned *status;  // device status word
-    // Work-unit scheduler of a persistent launch: sched[0] hands out unit indices (atomicAdd),
-    // sched[1] counts finished CTAs; the last CTA to finish sets both back to 0.
-    unsigned *sched;
+    unsigned *status;  // device status word of the launching stream
 };
-
-// Number of scheduler slots (two words each) in the library's static device array; a launch uses
-// slot (launch sequence number mod kSchedSlots), so only launches that many apart share one.
-constexpr int kSchedSlots = 1024;
-
-// Called by one thread of each CTA after the CTA's last use of the scheduler: the last CTA of the
-// launch resets the slot for the launch that reuses it.
-__device__ __forceinline__ void sched_release(const AttnParams &p) {
-    __threadfence();
-    if (atomicAdd(&p.sched[1], 1u) == gridDim.x - 1) {
-        atomicExch(&p.sched[0], 0u);
-        atomicExch(&p.sched[1], 0u);
-    }
-}
-
 
 // First allowed key of row r and one past its last, clamped to [0, S_k] (empty when lo >= hi).
 __device__ __forceinline__ int band_key_lo(const AttnParams &p, int r) {

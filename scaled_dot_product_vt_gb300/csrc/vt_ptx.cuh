@@ -189,6 +189,35 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- cluster launch control
+
+// Ask the hardware to cancel the launch of a CTA of this grid that has not started yet, so that this CTA can do
+// its work instead.  The 16-byte response lands at `resp` (shared, 16-byte aligned) and completes as 16
+// transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     resp),
+                 "r"(bar)
+                 : "memory");
+}
+
+// The x index of the CTA a completed request cancelled, or -1 when it cancelled none (every CTA of the grid
+// has started).
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "mov.u32 %1, 0;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok ? static_cast<int>(x) : -1;
+}
+
 // ---------------------------------------------------------------- thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -1,9 +1,9 @@
-"""The persistent bf16 kernel's work-unit counter: correct across many launches and concurrent streams.
+"""The persistent bf16 kernel's scheduling: correct across many launches, concurrent streams and graphs.
 
-Each launch draws its units from one slot of a static array of 1024 counters (launch sequence
-number mod 1024) and its last CTA resets the slot.  These tests check that the outputs stay
-bit-identical to a single reference launch when (a) more than 1024 launches wrap the slots
-around and (b) launches on two streams run at the same time (each on its own slot).
+A launch has one CTA per work unit; running CTAs take over the units of CTAs that have not started
+(cluster launch control), so no device state is shared between launches.  These tests check that the
+outputs stay bit-identical to a single reference launch over (a) 1100 launches in a row, (b) launches on
+two streams that run at the same time and (c) two captured CUDA graphs replayed on two streams at once.
 """
 
 from __future__ import annotations
@@ -35,8 +35,8 @@ def _inputs(seed, B=1, H=4, S=600):
     return q, k, v, float(np.float32(1.0 / math.sqrt(64)))
 
 
-def test_slots_wrap_around():
-    """1100 launches (more than the 1024 counter slots) in a row, all equal to the first."""
+def test_many_launches_in_a_row():
+    """1100 launches in a row, all equal to the first."""
     q, k, v, scale = _inputs(90)
     Q, K, V = to_device(q), to_device(k), to_device(v)
     ref = vt.attn_fwd(Q, K, V, scale=scale, causal=True)
@@ -71,3 +71,36 @@ def test_concurrent_streams():
     for i in range(20):
         assert torch.equal(outs1[i], ref1), f"stream 1 launch {i}"
         assert torch.equal(outs2[i], ref2), f"stream 2 launch {i}"
+
+
+def test_graphs_replayed_on_two_streams_at_once():
+    """Two captured forwards replayed concurrently on two streams, many times, give the eager results."""
+    q1, k1, v1, scale = _inputs(93, B=2, H=8, S=1200)
+    q2, k2, v2, _ = _inputs(94, B=2, H=8, S=1200)
+    Q1, K1, V1 = to_device(q1), to_device(k1), to_device(v1)
+    Q2, K2, V2 = to_device(q2), to_device(k2), to_device(v2)
+    ref1 = vt.attn_fwd(Q1, K1, V1, scale=scale, causal=True)
+    ref2 = vt.attn_fwd(Q2, K2, V2, scale=scale, causal=False)
+    torch.cuda.synchronize()
+    o1, o2 = torch.empty_like(ref1), torch.empty_like(ref2)
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        vt.attn_fwd(Q1, K1, V1, scale=scale, causal=True, out=o1)
+    with torch.cuda.graph(g2):
+        vt.attn_fwd(Q2, K2, V2, scale=scale, causal=False, out=o2)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    bad1 = torch.zeros((), dtype=torch.int64, device="cuda")
+    bad2 = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(50):
+        o1.zero_()
+        o2.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            g1.replay()
+        with torch.cuda.stream(s2):
+            g2.replay()
+        torch.cuda.synchronize()
+        bad1 += (o1 != ref1).sum()
+        bad2 += (o2 != ref2).sum()
+    assert vt.vt_last_device_status() == 0
+    assert int(bad1) == 0 and int(bad2) == 0
