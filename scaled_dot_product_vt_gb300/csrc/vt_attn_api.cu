@@ -377,10 +377,17 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         const unsigned grid = static_cast<unsigned>(units);
         // Q K^T K-steps of 16, rounded up to an even count (the TMA zero-fills past D_qk)
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
+        // value widths up to 64 leave TMEM room for the score ring (S of the next key tile during the softmax)
+        const bool ring = p.n_pv <= 64;
         void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
-            ksteps <= 2 ? attn_fwd_bf16_2q_kernel<2>
-                        : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4>
-                                      : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6> : attn_fwd_bf16_2q_kernel<8>;
+            ring ? (ksteps <= 2 ? attn_fwd_bf16_2q_kernel<2, true>
+                                : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, true>
+                                              : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, true>
+                                                            : attn_fwd_bf16_2q_kernel<8, true>)
+                 : (ksteps <= 2 ? attn_fwd_bf16_2q_kernel<2, false>
+                                : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, false>
+                                              : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, false>
+                                                            : attn_fwd_bf16_2q_kernel<8, false>);
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<grid, q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;

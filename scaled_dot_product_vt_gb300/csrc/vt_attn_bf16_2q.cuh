@@ -53,7 +53,7 @@ constexpr int kRegsSoftmax = 216;   // softmax warpgroups after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch");
 constexpr int kMaxSlots = 6;
 constexpr int kUnitRing = 4;        // unit indices in flight between the producer and the other roles
-constexpr int kUnitReaders = 1 + 8;  // the MMA thread and one lane of each softmax warp
+constexpr int kUnitReaders = 1 + 8;  // the MMA warp and one lane of each softmax warp (one more MMA warp with the score ring)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunk = 64;          // bf16 elements per 128-byte chunk
 constexpr uint32_t kChunkBytes = kBN * 128;  // one 128-byte column chunk of a 128-row tile
@@ -80,14 +80,17 @@ struct Ctl {
     uint64_t q_full;
     uint64_t q_empty;     // the unit's last Q K^T has read Q (the next unit's Q may be loaded)
     uint64_t s_full[2];   // scores of tile t ready (and every earlier MMA done)
-    uint64_t p_full[2];   // P of tile t written (128 arrivals)
+    uint64_t p_full[2][2];  // the h-th P of tile t written, on barrier [t][h mod 2] (128 arrivals): with the
+                            // score ring the softmax may hand over two P before the issuer takes the first
     uint64_t o_done[2];   // last P V of tile t done
+    uint64_t s_read[2];   // score ring: softmax t has the scores in registers (128 arrivals)
+    uint64_t o_ready[2][2];  // score ring: the c-th P V of tile t done, on barrier [t][c mod 2]
     uint64_t unit_full[kUnitRing];   // ring entry k written by the producer
     uint64_t unit_empty[kUnitRing];  // ring entry k read by every other role
     Unit unit[kUnitRing];            // decoded units (u = -1 once no CTA is left to take over)
     uint4 clc_resp;                  // response of the last launch-control request
     uint64_t clc_full;               // that response has landed
-    uint64_t drain;
+    uint64_t drain[2];  // a stopping MMA warp's products are done (one per MMA warp)
     uint64_t stall;
     uint32_t tmem_base;
     volatile uint32_t abort_flag;
@@ -191,7 +194,9 @@ __device__ __forceinline__ bool next_unit(Ctl &ctl, int n, Unit *out, const Attn
 }  // namespace q2
 
 // KQ: MMA K-steps (16 bf16 each) of Q K^T, D_qk rounded up: 2, 4, 6 or 8.
-template <int KQ>
+// RING: value widths up to 64, where TMEM holds a three-slot score ring per query tile (below), so the next
+// key tile's scores are computed while the softmax works on the current ones.
+template <int KQ, bool RING>
 __global__ void __launch_bounds__(q2::kThreads, 1)
     attn_fwd_bf16_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -216,22 +221,28 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
     const uint32_t sSlot0 = base + 2 * q_tile_bytes;
 
     if (threadIdx.x == 0) {
+        // with the score ring each query tile has its own MMA warp, and both release every slot and Q
         for (int s = 0; s < n_slots; ++s) {
             mbar_init(smem_u32(&ctl.full[s]), 1);
-            mbar_init(smem_u32(&ctl.empty[s]), 1);
+            mbar_init(smem_u32(&ctl.empty[s]), RING ? 2 : 1);
         }
         mbar_init(smem_u32(&ctl.q_full), 1);
-        mbar_init(smem_u32(&ctl.q_empty), 1);
+        mbar_init(smem_u32(&ctl.q_empty), RING ? 2 : 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&ctl.s_full[t]), 1);
-            mbar_init(smem_u32(&ctl.p_full[t]), 128);
+            mbar_init(smem_u32(&ctl.p_full[t][0]), 128);
+            mbar_init(smem_u32(&ctl.p_full[t][1]), 128);
             mbar_init(smem_u32(&ctl.o_done[t]), 1);
+            mbar_init(smem_u32(&ctl.s_read[t]), 128);
+            mbar_init(smem_u32(&ctl.o_ready[t][0]), 1);
+            mbar_init(smem_u32(&ctl.o_ready[t][1]), 1);
         }
         for (int k = 0; k < kUnitRing; ++k) {
             mbar_init(smem_u32(&ctl.unit_full[k]), 1);
-            mbar_init(smem_u32(&ctl.unit_empty[k]), kUnitReaders);
+            mbar_init(smem_u32(&ctl.unit_empty[k]), kUnitReaders + (RING ? 1 : 0));
         }
-        mbar_init(smem_u32(&ctl.drain), 1);
+        mbar_init(smem_u32(&ctl.drain[0]), 1);
+        mbar_init(smem_u32(&ctl.drain[1]), 1);
         mbar_init(smem_u32(&ctl.stall), 1);
         mbar_init(smem_u32(&ctl.clc_full), 1);
         ctl.abort_flag = 0;
@@ -356,8 +367,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     wait_drain(smem_u32(&ctl.full[k % n_slots]), (k / n_slots) & 1, p);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || (RING && warp == 2)) {
+        // ------------------------------------------------------------ MMA issuer(s)
         // The whole warp runs this code with warp-uniform values and waits on every barrier; one lane
         // chosen by elect.sync issues each MMA and commit.
         {
@@ -377,7 +388,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             const uint32_t o_col0 = tmem + col_o(0), o_col1 = tmem + col_o(1);
             bool ok = true, any_mma = false;
             uint32_t full_phase = 0;  // bit s: parity of the next full-phase of slot s
-            uint32_t p_par0 = 0, p_par1 = 0;  // parity of the next P hand-over of tile 0 / 1
+            uint32_t h0 = 0, h1 = 0;          // P hand-overs of tile 0 / 1 taken so far
             uint32_t q_par = 0;               // parity of the next Q load
 
             // K/V slots are filled by TMA: the mbarrier's completed transaction count already makes
@@ -406,6 +417,76 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
 
             if (p.flags & kFlagTestStall) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
             int ks = 0;  // slot of the next K tile (the ring runs on across units)
+            if constexpr (RING) {
+                // Score ring: tile t owns three 64-column TMEM slots from column 192 t, and O_t 64 columns from
+                // 384 + 64 t.  Its g-th scores (counted over the CTA's life) sit in slots 0-1 for even g and
+                // slots 1-2 for odd g, and their P overwrites slot 0 or slot 2, so the next scores never touch
+                // the P still to be multiplied.  Warp 1 issues tile 0's products and warp 2 tile 1's, so one
+                // tile's chain never waits behind the other's.  S_t = Q_t K_{j+1}^T is issued once softmax t
+                // has read the scores of key tile j (s_read), ahead of P_t,j V_j; each P V commits
+                // o_ready[t][c mod 2] (c: the tile's P V count), which the softmax consumes before it rescales
+                // O_t and before the epilogue.  Both warps release every K/V slot and Q (two arrivals each).
+                const int tm = warp - 1;
+                const uint32_t s_reg = tmem + static_cast<uint32_t>(tm * 192);
+                const uint32_t o_r = tmem + static_cast<uint32_t>(384 + tm * 64);
+                const uint32_t q_lo = tm ? q_lo1 : q_lo0;
+                auto s_at = [&](uint32_t gi) { return s_reg + ((gi & 1u) ? 64u : 0u); };
+                auto p_at = [&](uint32_t gi) { return s_reg + ((gi & 1u) ? 128u : 0u); };
+                uint32_t g = 0, cur = 0, nxt = 0, c = 0, h = 0, sr_par = 0;
+                for (int n = 0; ok; ++n) {
+                    Unit U;
+                    if (!(ok = next_unit(ctl, n, &U, p, lane)) || U.u < 0) break;
+                    const int n_kv = U.n_kv;
+                    if (n_kv == 0) continue;
+                    const int as = tm ? U.as1 : U.as0, es = tm ? U.es1 : U.es0;
+                    // this tile takes part in key tile j when as <= j < es
+                    auto act = [&](int j) { return j >= as && j < es; };
+                    if (!(ok = wait1(smem_u32(&ctl.q_full), q_par))) break;
+                    q_par ^= 1u;
+                    if (!(ok = wait_full(ks))) break;
+                    if (act(0)) {
+                        cur = g++;
+                        qk(s_at(cur), q_lo, k_lo0 + ks * slot_step);
+                        mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                        any_mma = true;
+                    }
+                    if (es <= 1) mma_commit_elect(smem_u32(&ctl.q_empty));  // this tile's last Q K^T (or none)
+                    mma_commit_elect(smem_u32(&ctl.empty[ks]));
+                    for (int j = 0; ok && j < n_kv; ++j) {
+                        const int vs = ks + 1 == n_slots ? 0 : ks + 1;  // slot of V_j
+                        const int kn = vs + 1 == n_slots ? 0 : vs + 1;  // slot of K_{j+1} (or the next unit's K_0)
+                        if (j + 1 < n_kv) {
+                            // the next key tile's scores, as soon as the softmax holds the current ones
+                            if (!(ok = wait_full(kn))) break;
+                            if (act(j + 1)) {
+                                if (act(j)) {
+                                    if (!(ok = wait1(smem_u32(&ctl.s_read[tm]), sr_par))) break;
+                                    sr_par ^= 1u;
+                                    tc_fence_after();
+                                }
+                                nxt = g++;
+                                qk(s_at(nxt), q_lo, k_lo0 + kn * slot_step);
+                                mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                                any_mma = true;
+                                if (j + 2 == es) mma_commit_elect(smem_u32(&ctl.q_empty));  // this tile's last Q K^T
+                            }
+                            mma_commit_elect(smem_u32(&ctl.empty[kn]));
+                        }
+                        if (!(ok = wait_full(vs))) break;
+                        if (act(j)) {
+                            if (!(ok = wait1(smem_u32(&ctl.p_full[tm][h & 1u]), (h >> 1) & 1u))) break;
+                            ++h;
+                            tc_fence_after();
+                            pv(o_r, p_at(cur), v_lo0 + vs * slot_step, j > as);
+                            mma_commit_elect(smem_u32(&ctl.o_ready[tm][c & 1u]));
+                            ++c;
+                        }
+                        if (act(j + 1)) cur = nxt;  // the scores (and P) of key tile j + 1
+                        mma_commit_elect(smem_u32(&ctl.empty[vs]));
+                        ks = kn;
+                    }
+                }
+            } else {
             for (int n = 0; ok; ++n) {
                 Unit U;
                 if (!(ok = next_unit(ctl, n, &U, p, lane)) || U.u < 0) break;
@@ -440,8 +521,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     const uint32_t v_lo = v_lo0 + vs * slot_step;
                     const uint32_t kn_lo = k_lo0 + kn * slot_step;
                     if (act0(j)) {
-                        if (!(ok = wait1(smem_u32(&ctl.p_full[0]), p_par0))) break;
-                        p_par0 ^= 1u;
+                        if (!(ok = wait1(smem_u32(&ctl.p_full[0][h0 & 1u]), (h0 >> 1) & 1u))) break;
+                        ++h0;
                         tc_fence_after();
                         pv(o_col0, s_col0, v_lo, j > as0);
                     }
@@ -453,8 +534,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                         mma_commit_elect(smem_u32(&ctl.o_done[0]));
                     }
                     if (act1(j)) {
-                        if (!(ok = wait1(smem_u32(&ctl.p_full[1]), p_par1))) break;
-                        p_par1 ^= 1u;
+                        if (!(ok = wait1(smem_u32(&ctl.p_full[1][h1 & 1u]), (h1 >> 1) & 1u))) break;
+                        ++h1;
                         tc_fence_after();
                         pv(o_col1, s_col1, v_lo, j > as1);
                     }
@@ -470,9 +551,10 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     ks = kn;
                 }
             }
+            }
             if (!ok && any_mma) {
-                mma_commit_elect(smem_u32(&ctl.drain));
-                if (lane == 0) wait_drain(smem_u32(&ctl.drain), 0, p);
+                mma_commit_elect(smem_u32(&ctl.drain[warp - 1]));
+                if (lane == 0) wait_drain(smem_u32(&ctl.drain[warp - 1]), 0, p);
                 __syncwarp();
             }
         }
@@ -484,14 +566,24 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         const int quad = warp & 3;                  // TMEM lane quadrant
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + col_s(t);
-        const uint32_t o_addr = tmem + lane_base + col_o(t);
+        // score ring: slots from column 192 t, O_t at 384 + 64 t (see the MMA issuer); otherwise S_t and O_t
+        const uint32_t s_base = tmem + lane_base + (RING ? static_cast<uint32_t>(t * 192) : col_s(t));
+        const uint32_t o_addr = tmem + lane_base + (RING ? static_cast<uint32_t>(384 + t * 64) : col_o(t));
         // Non-positive scales are applied to the scores first, so the folded form below sees c > 0.
         const bool fold = p.scale_log2 > 0.0f;
         const float c = fold ? p.scale_log2 : 1.0f;
         const float2 c2 = make_float2(c, c);
         uint32_t s_par = 0, o_par = 0;  // parities of the next scores and the next o_done of this tile
+        uint32_t g = 0;                 // score ring: scores of this tile seen over the CTA's life
+        uint32_t handed = 0;            // P hand-overs of this tile over the CTA's life
+        uint32_t pv_handed = 0, pv_seen = 0;  // score ring: P hand-overs, and P V completions consumed
         bool ok = true;
+        // score ring: consume the completion of the oldest P V not yet consumed
+        auto wait_pv = [&]() -> bool {
+            const bool r = wait_bounded(smem_u32(&ctl.o_ready[t][pv_seen & 1u]), (pv_seen >> 1) & 1u, ctl.abort_flag, p);
+            ++pv_seen;
+            return __all_sync(0xffffffffu, r) != 0;
+        };
 
         for (int n = 0; ok; ++n) {
             Unit U;
@@ -515,10 +607,16 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t s_addr = s_base + ((RING && (g & 1u)) ? 64u : 0u);   // scores
+                const uint32_t p_addr = s_base + ((RING && (g & 1u)) ? 128u : 0u);  // P over them
                 uint32_t sr[BN];
                 #pragma unroll
                 for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(s_addr + cc * 32, sr + cc * 32);
                 tmem_wait_ld();
+                if (RING && j + 1 < n_my) {  // the next scores may now be written over these
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&ctl.s_read[t]));
+                }
                 float s[BN];
                 #pragma unroll
                 for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
@@ -580,13 +678,19 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                         pk[k / 2] = pack_bf16x2(e0.x, e0.y);
                         pk[k / 2 + 1] = pack_bf16x2(e1.x, e1.y);
                     }
-                    tmem_st16(s_addr + cc / 2, pk);
+                    tmem_st16(p_addr + cc / 2, pk);
                 }
                 l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 // O_t *= alpha where the reference moved (after the scores are dead, to keep registers
                 // low).  The scores just read were committed after P_t,j-1 V_j-1, so O_t holds its final
                 // value for tile j-1 and no MMA touches it now.
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                    if (RING) {  // O_t must hold every P V handed over so far
+                        bool w = true;
+                        while (w && pv_seen < pv_handed) w = wait_pv();
+                        if (!(ok = w)) break;
+                        tc_fence_after();
+                    }
                     for (int cc = 0; cc < p.n_pv; cc += 32) {
                         uint32_t o[32];
                         tmem_ld32(o_addr + cc, o);
@@ -598,13 +702,23 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(smem_u32(&ctl.p_full[t]));
+                mbar_arrive(smem_u32(&ctl.p_full[t][handed & 1u]));
+                ++handed;
+                if (RING) {
+                    ++pv_handed;
+                    ++g;
+                    if (pv_handed - pv_seen >= 2 && !(ok = wait_pv())) break;  // at most one P V outstanding
+                }
             }
 
             if (ok && n_my > 0) {
-                ok = wait_bounded(smem_u32(&ctl.o_done[t]), o_par, ctl.abort_flag, p);
-                o_par ^= 1u;
-                ok = __all_sync(0xffffffffu, ok);
+                if (RING) {
+                    while (ok && pv_seen < pv_handed) ok = wait_pv();
+                } else {
+                    ok = wait_bounded(smem_u32(&ctl.o_done[t]), o_par, ctl.abort_flag, p);
+                    o_par ^= 1u;
+                    ok = __all_sync(0xffffffffu, ok);
+                }
             }
             const bool row_ok = q_row < p.S_q;
             if (ok && p.n_split == 1) {
