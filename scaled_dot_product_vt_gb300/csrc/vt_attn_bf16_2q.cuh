@@ -319,6 +319,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 mbar_arrive(smem_u32(&ctl.unit_full[k]));
                 if (u < 0) break;
                 if (U.n_kv == 0) continue;
+                // The unit's Q may only be loaded once the previous unit's last Q K^T has read the Q buffers;
+                // fetch it into L2 now, so that the load after that point is an L2 hit.
+                for (int t = 0; t < 2; ++t)
+                    if ((t ? U.es1 > U.as1 : U.es0 > U.as0))
+                        for (int c = 0; c < p.q_chunks; ++c) tma_prefetch_l2_4d(&tmQ, c * kChunk, U.r0 + t * kBM, U.h, U.b);
                 if (q_loads > 0) {  // the previous unit's last Q K^T has read Q
                     ok = wait_bounded(smem_u32(&ctl.q_empty), (q_loads - 1) & 1, ctl.abort_flag, p);
                     if (!ok) break;

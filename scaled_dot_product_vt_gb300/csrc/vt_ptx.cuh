@@ -64,6 +64,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Prefetch one box of a 4-D tiled tensor into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
