@@ -1,6 +1,6 @@
 // Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per work unit sharing every
-// 128-key K/V tile, one softmax warpgroup per query tile, tcgen05 issued by one warp (one lane
-// elected per instruction).
+// 128-key K/V tile, one softmax warpgroup per query tile, tcgen05 issued by one warp (two warps, one
+// per query tile, for value widths up to 64), one lane elected per instruction.
 //
 // Persistent through cluster launch control: the grid has one CTA per work unit, but a running CTA
 // takes over the units of CTAs that have not started yet (clusterlaunchcontrol.try_cancel), so about
@@ -22,17 +22,26 @@
 //                tile.  Every operand descriptor is computed once; the K-steps are unrolled
 //                (a per-instruction descriptor computation made the issuing thread, not the
 //                tensor core, the bottleneck).
-//   warps 2-3    idle (they complete warpgroup 0, which gives registers to the softmax warpgroups)
+//                For value widths up to 64 (the score-ring variant) warp 1 issues for tile 0 and
+//                warp 2 for tile 1, each one key tile ahead: S_t = Q_t K_{j+1}^T goes into a free
+//                slot of tile t's ring while softmax t still works on S_t,j.
+//   warps 2-3    idle (they complete warpgroup 0, which gives registers to the softmax warpgroups);
+//                warp 2 is tile 1's issuer in the score-ring variant
 //   warps 4-7    softmax warpgroup of tile 0, one row per thread (TMEM lane quadrant = warp % 4)
 //   warps 8-11   softmax warpgroup of tile 1
 // Registers: launched at 168 per thread; warpgroup 0 shrinks to 72 and the softmax warpgroups
 // grow to 216 (128 x 72 + 256 x 216 = 384 x 168, so the increase never waits on a shortfall).
-// TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each.  P_t,j overwrites S_t,j as bf16
-// pairs (64 columns) and is read from TMEM by the P V product.  A commit after S_t = Q_t K^T
+// TMEM (512 columns): S_0, S_1, O_0, O_1, 128 columns each (score ring: three 64-column score
+// slots per tile at columns 0-191 and 192-383, O_0 and O_1 at 384 and 448; even key tiles put S in
+// slots 0-1 and P in slot 0, odd ones S in slots 1-2 and P in slot 2, so the next scores never land
+// on a P still being read).  P_t,j overwrites S_t,j as bf16
+// pairs (64 columns) and is read from TMEM by the P V product.  Without the ring, a commit after S_t = Q_t K^T
 // also covers the P V issued before it, so when softmax t sees its next scores, O_t is final
 // for the previous tile and may be rescaled in place.  Softmax t reads O_t for a unit's epilogue
 // before it hands over the next unit's first P_t, and the first P_t V of a unit (which overwrites
-// O_t) waits for that hand-over: no separate barrier guards O_t between units.
+// O_t) waits for that hand-over: no separate barrier guards O_t between units.  With the ring the
+// scores run a key tile ahead of P V, so each P V instead commits its own barrier (o_ready), and the
+// softmax waits on it before rescaling O_t or reading it for the epilogue.
 //
 // The decomposition (query block, head, batch), the tail masks and the write set follow the
 // FA-1 boundary kernel verified on the VeriTile page "VeriTile.Examples.FlashAttention1.
