@@ -320,6 +320,10 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
     p.o_sb = os[0];
     p.o_sh = os[1];
     p.o_ss = os[2];
+    p.o_vec32 = (reinterpret_cast<uintptr_t>(O) % 32 == 0 && (os[0] * C::kElt) % 32 == 0 &&
+                 (os[1] * C::kElt) % 32 == 0 && (os[2] * C::kElt) % 32 == 0)
+                    ? 1
+                    : 0;
     p.V = V;
     p.v_sb = vs[0];
     p.v_sh = vs[1];

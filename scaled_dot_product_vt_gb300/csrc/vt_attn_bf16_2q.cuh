@@ -758,9 +758,13 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     for (int k = 0; k < 8; ++k)
                         w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
                     if (cc + 16 <= p.D_v) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        if (p.o_vec32) {  // half as many store instructions, each a full 32-byte sector
+                            st_global_v8(orow + cc * 2, w);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 2);
+                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
                     } else {
                         uint16_t *dst = reinterpret_cast<uint16_t *>(orow) + cc;
                         #pragma unroll

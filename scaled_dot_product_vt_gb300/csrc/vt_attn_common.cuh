@@ -39,6 +39,7 @@ struct AttnParams {
     float *lse;        // nullptr, or [B*H*S_q] natural-log log-sum-exp per row
     void *O;
     long long o_sb, o_sh, o_ss;  // element strides of O for b, h, s
+    int o_vec32;                 // 1: O and its strides are 32-byte multiples (32-byte stores of O rows)
     const void *V;               // read by the fp32 V loader
     long long v_sb, v_sh, v_ss;
     const void *Q;               // read by the fp32 kernel's softmax threads (Q goes to TMEM)

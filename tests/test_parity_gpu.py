@@ -178,8 +178,10 @@ SENT32 = 0x7FC0DEAD
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_write_set_guard_bands(dtype, causal):
-    """Only O[b,h,i<S_q,e<D_v] is written: padding columns, padding rows and 4 KiB canaries stay bit-exact."""
+@pytest.mark.parametrize("shift", [0, 16])
+def test_write_set_guard_bands(dtype, causal, shift):
+    """Only O[b,h,i<S_q,e<D_v] is written: padding columns, padding rows and 4 KiB canaries stay bit-exact.
+    shift = 16 starts O 16 bytes past a 32-byte boundary (the bf16 epilogue then stores 16 bytes at a time)."""
     B, H, S_q, S_k, D_qk, D_v = 2, 3, 201, 150, 40, 24
     q, k, v = synth.make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype, seed=14)
     elt = 2 if dtype == "bf16" else 4
@@ -187,18 +189,19 @@ def test_write_set_guard_bands(dtype, causal):
     row = D_v + pad_d
     o_strides = (H * (S_q + pad_s) * row, (S_q + pad_s) * row, row)
     canary = 4096 // elt
-    total = canary + B * o_strides[0] + canary
+    total = canary + B * o_strides[0] + canary + 16
     tdt = torch.int16 if dtype == "bf16" else torch.int32
     sentinel = SENT16 - (1 << 16) if dtype == "bf16" else SENT32
     buf = torch.full((total,), sentinel, dtype=tdt, device="cuda")
     view_dt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    O = torch.as_strided(buf.view(view_dt), (B, H, S_q, D_v), o_strides + (1,), canary + row)  # after one pad row
+    o0 = canary + row + shift // elt  # after one pad row
+    O = torch.as_strided(buf.view(view_dt), (B, H, S_q, D_v), o_strides + (1,), o0)
     Q, K, V = to_device(q), to_device(k), to_device(v)
     vt.attn_fwd(Q, K, V, scale=0.2, causal=causal, out=O)
     assert vt.vt_last_device_status() == 0
     host = buf.cpu().numpy()
     mask = np.ones(total, bool)
-    idx = (canary + row + np.arange(B)[:, None, None, None] * o_strides[0] + np.arange(H)[None, :, None, None] * o_strides[1]
+    idx = (o0 + np.arange(B)[:, None, None, None] * o_strides[0] + np.arange(H)[None, :, None, None] * o_strides[1]
            + np.arange(S_q)[None, None, :, None] * o_strides[2] + np.arange(D_v)[None, None, None, :])
     mask[idx.ravel()] = False
     assert np.all(host[mask] == sentinel), "a position outside O's logical elements was written"
