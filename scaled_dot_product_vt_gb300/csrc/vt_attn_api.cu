@@ -195,7 +195,8 @@ bool make_map(CUtensorMap *map, const void *ptr, const int64_t st[3], int64_t B,
     return r == CUDA_SUCCESS;
 }
 
-// Workspace of a split-KV call: partial outputs, then row maxima, then row sums (256-byte aligned).
+// Workspace of a split-KV call: partial outputs, then row maxima, row sums and row-sum corrections
+// (each part 256-byte aligned).
 struct SplitLayout {
     size_t o_off, m_off, l_off, c_off, bytes;
 };

@@ -417,16 +417,18 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 return r;
             };
             auto qk = [&](uint32_t d, uint32_t q_lo, uint32_t k_lo) {
+                const uint32_t lead = elect_leader();
 #pragma unroll
                 for (int kk = 0; kk < KQ; ++kk) {
                     const uint32_t off = (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2;
-                    mma_ss_elect(d, q_lo + off, q_hi, k_lo + off, k_hi, idesc_qk, kk > 0);
+                    mma_ss_lead(d, q_lo + off, q_hi, k_lo + off, k_hi, idesc_qk, kk > 0, lead);
                 }
             };
             auto pv = [&](uint32_t d, uint32_t a, uint32_t v_lo, uint32_t acc0) {
+                const uint32_t lead = elect_leader();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts_elect(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u);
+                    mma_ts_lead(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u, lead);
             };
 
             if (p.flags & kFlagTestStall) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook
