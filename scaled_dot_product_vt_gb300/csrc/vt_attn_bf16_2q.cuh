@@ -1,6 +1,6 @@
 // Attention forward, bf16 I/O, for sm_103a: two 128-row query tiles per work unit sharing every
 // 128-key K/V tile, one softmax warpgroup per query tile, tcgen05 issued by one warp (two warps, one
-// per query tile, for value widths up to 64), one lane elected per instruction.
+// per query tile, for value widths up to 64), one lane (elected once) issuing every MMA and commit.
 //
 // Persistent through cluster launch control: the grid has one CTA per work unit, but a running CTA
 // takes over the units of CTAs that have not started yet (clusterlaunchcontrol.try_cancel), so about
@@ -16,7 +16,7 @@
 //                Q K^T has read Q), then K_0, V_0, K_1, V_1, ... through a ring of equal
 //                shared-memory slots (mbarrier full/empty per slot) that runs on across units.
 //   warp 1       TMEM owner and MMA issuer (the whole warp runs the issuing code with warp-uniform
-//                values; one elected lane issues).  Per key tile j the tensor core runs
+//                values; one lane, elected once, issues).  Per key tile j the tensor core runs
 //                  O_0 += P_0,j V_j,  S_0 = Q_0 K_{j+1}^T,  O_1 += P_1,j V_j,  S_1 = Q_1 K_{j+1}^T
 //                so while softmax warpgroup t works on S_t, the tensor core works for the other
 //                tile.  Every operand descriptor is computed once; the K-steps are unrolled
@@ -383,8 +383,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         }
     } else if (warp == 1 || (RING && warp == 2)) {
         // ------------------------------------------------------------ MMA issuer(s)
-        // The whole warp runs this code with warp-uniform values and waits on every barrier; one lane
-        // chosen by elect.sync issues each MMA and commit.
+        // The whole warp runs this code with warp-uniform values and waits on every barrier; one lane,
+        // chosen once by elect.sync, issues every MMA and commit (as a predicate, the warp stays converged).
         {
             const uint32_t idesc_qk = instr_desc(1, kBM, BN, 0);
             const uint32_t idesc_pv = instr_desc(1, kBM, p.n_pv, 1);
@@ -404,10 +404,13 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
             uint32_t full_phase = 0;  // bit s: parity of the next full-phase of slot s
             uint32_t h0 = 0, h1 = 0;          // P hand-overs of tile 0 / 1 taken so far
             uint32_t q_par = 0;               // parity of the next Q load
+            // The lane that issues every MMA and commit of this warp, elected once: a commit tracks the MMAs
+            // of the thread that issues it, so all of them come from this one lane.
+            const uint32_t lead = elect_leader();
 
             // K/V slots are filled by TMA: the mbarrier's completed transaction count already makes
             // the bytes visible to the tensor core, so no tcgen05 fence is needed after this wait.
-            // Every lane waits, so whichever lane elect.sync picks has itself observed the phase.
+            // Every lane waits, so the issuing lane has itself observed the phase.
             auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl.abort_flag, p)) != 0;
             };
@@ -417,7 +420,6 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 return r;
             };
             auto qk = [&](uint32_t d, uint32_t q_lo, uint32_t k_lo) {
-                const uint32_t lead = elect_leader();
 #pragma unroll
                 for (int kk = 0; kk < KQ; ++kk) {
                     const uint32_t off = (kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2;
@@ -425,7 +427,6 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
             };
             auto pv = [&](uint32_t d, uint32_t a, uint32_t v_lo, uint32_t acc0) {
-                const uint32_t lead = elect_leader();
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts_lead(d, a + kk * 8, v_lo + kk * 128, v_hi, idesc_pv, (acc0 | kk) ? 1u : 0u, lead);
@@ -463,11 +464,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     if (act(0)) {
                         cur = g++;
                         qk(s_at(cur), q_lo, k_lo0 + ks * slot_step);
-                        mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[tm]), lead);
                         any_mma = true;
                     }
-                    if (es <= 1) mma_commit_elect(smem_u32(&ctl.q_empty));  // this tile's last Q K^T (or none)
-                    mma_commit_elect(smem_u32(&ctl.empty[ks]));
+                    if (es <= 1) mma_commit_lead(smem_u32(&ctl.q_empty), lead);  // this tile's last Q K^T (or none)
+                    mma_commit_lead(smem_u32(&ctl.empty[ks]), lead);
                     for (int j = 0; ok && j < n_kv; ++j) {
                         const int vs = ks + 1 == n_slots ? 0 : ks + 1;  // slot of V_j
                         const int kn = vs + 1 == n_slots ? 0 : vs + 1;  // slot of K_{j+1} (or the next unit's K_0)
@@ -482,11 +483,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                                 }
                                 nxt = g++;
                                 qk(s_at(nxt), q_lo, k_lo0 + kn * slot_step);
-                                mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                                mma_commit_lead(smem_u32(&ctl.s_full[tm]), lead);
                                 any_mma = true;
-                                if (j + 2 == es) mma_commit_elect(smem_u32(&ctl.q_empty));  // this tile's last Q K^T
+                                if (j + 2 == es) mma_commit_lead(smem_u32(&ctl.q_empty), lead);  // this tile's last Q K^T
                             }
-                            mma_commit_elect(smem_u32(&ctl.empty[kn]));
+                            mma_commit_lead(smem_u32(&ctl.empty[kn]), lead);
                         }
                         if (!(ok = wait_full(vs))) break;
                         if (act(j)) {
@@ -494,11 +495,11 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                             ++h;
                             tc_fence_after();
                             pv(o_r, p_at(cur), v_lo0 + vs * slot_step, j > as);
-                            mma_commit_elect(smem_u32(&ctl.o_ready[tm][c & 1u]));
+                            mma_commit_lead(smem_u32(&ctl.o_ready[tm][c & 1u]), lead);
                             ++c;
                         }
                         if (act(j + 1)) cur = nxt;  // the scores (and P) of key tile j + 1
-                        mma_commit_elect(smem_u32(&ctl.empty[vs]));
+                        mma_commit_lead(smem_u32(&ctl.empty[vs]), lead);
                         ks = kn;
                     }
                 }
@@ -519,14 +520,14 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     const uint32_t k_lo = k_lo0 + ks * slot_step;
                     if (act0(0)) {
                         qk(s_col0, q_lo0, k_lo);
-                        mma_commit_elect(smem_u32(&ctl.s_full[0]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[0]), lead);
                     }
                     if (act1(0)) {
                         qk(s_col1, q_lo1, k_lo);
-                        mma_commit_elect(smem_u32(&ctl.s_full[1]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[1]), lead);
                     }
-                    if (n_kv == 1) mma_commit_elect(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
-                    mma_commit_elect(smem_u32(&ctl.empty[ks]));
+                    if (n_kv == 1) mma_commit_lead(smem_u32(&ctl.q_empty), lead);  // last Q K^T of the unit
+                    mma_commit_lead(smem_u32(&ctl.empty[ks]), lead);
                     any_mma = true;
                 }
                 for (int j = 0; ok && j < n_kv; ++j) {
@@ -545,9 +546,9 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     if (more && !(ok = wait_full(kn))) break;
                     if (act0(j + 1)) {
                         qk(s_col0, q_lo0, kn_lo);
-                        mma_commit_elect(smem_u32(&ctl.s_full[0]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[0]), lead);
                     } else if (act0(j)) {
-                        mma_commit_elect(smem_u32(&ctl.o_done[0]));
+                        mma_commit_lead(smem_u32(&ctl.o_done[0]), lead);
                     }
                     if (act1(j)) {
                         if (!(ok = wait1(smem_u32(&ctl.p_full[1][h1 & 1u]), (h1 >> 1) & 1u))) break;
@@ -555,21 +556,21 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                         tc_fence_after();
                         pv(o_col1, s_col1, v_lo, j > as1);
                     }
-                    mma_commit_elect(smem_u32(&ctl.empty[vs]));
+                    mma_commit_lead(smem_u32(&ctl.empty[vs]), lead);
                     if (act1(j + 1)) {
                         qk(s_col1, q_lo1, kn_lo);
-                        mma_commit_elect(smem_u32(&ctl.s_full[1]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[1]), lead);
                     } else if (act1(j)) {
-                        mma_commit_elect(smem_u32(&ctl.o_done[1]));
+                        mma_commit_lead(smem_u32(&ctl.o_done[1]), lead);
                     }
-                    if (j + 2 == n_kv) mma_commit_elect(smem_u32(&ctl.q_empty));  // last Q K^T of the unit
-                    if (more) mma_commit_elect(smem_u32(&ctl.empty[kn]));
+                    if (j + 2 == n_kv) mma_commit_lead(smem_u32(&ctl.q_empty), lead);  // last Q K^T of the unit
+                    if (more) mma_commit_lead(smem_u32(&ctl.empty[kn]), lead);
                     ks = kn;
                 }
             }
             }
             if (!ok && any_mma) {
-                mma_commit_elect(smem_u32(&ctl.drain[warp - 1]));
+                mma_commit_lead(smem_u32(&ctl.drain[warp - 1]), lead);
                 if (lane == 0) wait_drain(smem_u32(&ctl.drain[warp - 1]), 0, p);
                 __syncwarp();
             }

@@ -145,6 +145,17 @@ __device__ __forceinline__ void mma_ts_lead(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// tcgen05.commit by the lanes where `leader` is set (see elect_leader): `bar` gets one arrival once every
+// tcgen05 MMA that lane issued so far has completed.
+__device__ __forceinline__ void mma_commit_lead(uint32_t bar, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred l;\n\t"
+        "setp.ne.b32 l, %1, 0;\n\t"
+        "@l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(leader)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 MMA issued so far by this thread has completed (warp-collective,
 // one elected lane issues).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
