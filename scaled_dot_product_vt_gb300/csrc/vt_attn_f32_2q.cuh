@@ -18,7 +18,7 @@
 // Warp roles (16 warps):
 //   warp 0              TMA producer: K_j and V_j into stage j of a ring of stages
 //   warps 1 / 13        MMA issuers of query tiles 0 / 1 (warp 1 also owns TMEM); each whole warp runs the
-//                       issuing code with warp-uniform values and one elected lane issues.  Per key tile j
+//                       issuing code with warp-uniform values and one lane, elected once, issues.  Per key tile j
 //                       of its range:  O_t += P_t,j V_j,  S_t = Q_t K_{j+1}^T
 //   warps 4-7 / 8-11    softmax warpgroups of query tiles 0 / 1, one row per thread: each first copies its
 //                       row of Q from shared memory into TMEM, then runs the online softmax and the epilogue
@@ -300,7 +300,9 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
             const uint32_t s_col = tmem + col_s0 + tm * BN, o_col = tmem + col_o0 + tm * p.n_pv;
             const uint32_t q_col = tmem + col_q0 + tm * dq;
             bool any_mma = false;
-            // Every lane waits, so whichever lane elect.sync picks has itself observed the phase.
+            // The lane that issues every MMA and commit of this warp, elected once (a commit tracks the MMAs of
+            // the thread that issues it).  Every lane waits, so the issuing lane has itself observed the phase.
+            const uint32_t lead = elect_leader();
             auto wait1 = [&](uint32_t bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl.abort_flag, p)) != 0;
             };
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
 #define VT_QK_STEP(kk)                                                                                             \
     case (kk) + 1:                                                                                                 \
         if ((kk) < KQ) {                                                                                           \
-            mma_ts_tf32_elect(s_col, q_col + (kk) * 8, k_lo + ((kk) >> 2) * (BN * 8) + ((kk) & 3) * 2, k_hi,        \
-                              idesc_qk, acc);                                                                      \
+            mma_ts_tf32_lead(s_col, q_col + (kk) * 8, k_lo + ((kk) >> 2) * (BN * 8) + ((kk) & 3) * 2, k_hi,         \
+                             idesc_qk, acc, lead);                                                                 \
             acc = 1;                                                                                               \
         }
                 switch (ksteps) {
@@ -330,8 +332,8 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
                 const uint32_t v_lo = v_lo0 + (j % p.stages) * stage_step;
 #pragma unroll
                 for (int kk = 0; kk < BN / 8; ++kk)
-                    mma_ts_tf32_elect(o_col, s_col + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi, idesc_pv,
-                                      (acc0 | kk) ? 1u : 0u);
+                    mma_ts_tf32_lead(o_col, s_col + kk * 8, v_lo + (kk >> 2) * v_chunk + (kk & 3) * 2, v_hi, idesc_pv,
+                                     (acc0 | kk) ? 1u : 0u, lead);
             };
 
             if (p.flags & kFlagTestStall) ok = wait1(smem_u32(&ctl.stall), 0);  // test hook: never signalled
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
                 if (ok) ok = wait1(smem_u32(&ctl.full_k[as % p.stages]), (as / p.stages) & 1);
                 if (ok) {
                     qk(as);
-                    mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                    mma_commit_lead(smem_u32(&ctl.s_full[tm]), lead);
                 }
             }
             uint32_t p_par = 0;
@@ -360,12 +362,12 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
                     if (j + 1 < es) {
                         if (!(ok = wait1(smem_u32(&ctl.full_k[(j + 1) % p.stages]), ((j + 1) / p.stages) & 1))) break;
                         qk(j + 1);
-                        mma_commit_elect(smem_u32(&ctl.s_full[tm]));
+                        mma_commit_lead(smem_u32(&ctl.s_full[tm]), lead);
                     } else {
-                        mma_commit_elect(smem_u32(&ctl.o_done[tm]));
+                        mma_commit_lead(smem_u32(&ctl.o_done[tm]), lead);
                     }
                 }
-                mma_commit_elect(smem_u32(&ctl.empty[st]));  // this tile is done with stage st
+                mma_commit_lead(smem_u32(&ctl.empty[st]), lead);  // this tile is done with stage st
                 if (tm == 0) {
                     __syncwarp();
                     if (lane == 0) ctl.t0_issued = static_cast<uint32_t>(j + 1);
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
             }
             if (tm == 0 && lane == 0) ctl.t0_issued = 0x7FFFFFFFu;  // stopped or done: never hold tile 1 back
             if (!ok && any_mma) {
-                mma_commit_elect(smem_u32(&ctl.drain[tm]));
+                mma_commit_lead(smem_u32(&ctl.drain[tm]), lead);
                 if (lane == 0) wait_drain(smem_u32(&ctl.drain[tm]), 0, p);
                 __syncwarp();
             }

@@ -92,26 +92,12 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A * B in TF32, A from TMEM and B from a shared-memory descriptor passed as its (low, high)
-// 32-bit words (operand offsets only change the low word).  Warp-collective: every lane of the warp executes
-// the call with the same (warp-uniform) operands, and one lane chosen by elect.sync issues the instruction.
-// Keeping the issuing code warp-uniform lets the operands stay in uniform registers.
-__device__ __forceinline__ void mma_ts_tf32_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
-                                                  uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "mov.b64 db, {%2, %3};\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// bf16 MMAs, D[tmem] (+)= A * B with A from a shared-memory descriptor (ss) or from TMEM (ts), issued as a
-// group under one election: elect_leader() is 1 in the lane elect.sync picks and 0 in the others, and the
-// *_lead forms issue in the lanes where `leader` is set (the warp stays converged, its operands uniform).
-// One election per group instead of one per instruction leaves more issue slots to the other warps of the
-// sub-partition.
+// MMAs D[tmem] (+)= A * B, bf16 with A from a shared-memory descriptor (ss) or from TMEM (ts), TF32 with A from
+// TMEM; B from a shared-memory descriptor passed as its (low, high) 32-bit words (operand offsets only change
+// the low word).  Warp-collective: every lane executes the call with the same warp-uniform operands, and only
+// the lane where `leader` is set issues.  elect_leader() is 1 in the lane elect.sync picks and 0 in the others;
+// an issuing warp elects once and keeps that lane for every MMA and commit (a commit tracks the MMAs of its
+// own thread), which also spares an election per instruction.
 __device__ __forceinline__ uint32_t elect_leader() {
     uint32_t r;
     asm volatile(
@@ -145,6 +131,17 @@ __device__ __forceinline__ void mma_ts_lead(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+__device__ __forceinline__ void mma_ts_tf32_lead(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                 uint32_t idesc, uint32_t accumulate, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred p, l;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 l, %6, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "@l tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
 // tcgen05.commit by the lanes where `leader` is set (see elect_leader): `bar` gets one arrival once every
 // tcgen05 MMA that lane issued so far has completed.
 __device__ __forceinline__ void mma_commit_lead(uint32_t bar, uint32_t leader) {
@@ -156,15 +153,6 @@ __device__ __forceinline__ void mma_commit_lead(uint32_t bar, uint32_t leader) {
         : "memory");
 }
 
-// Arrive (once) on `bar` when every tcgen05 MMA issued so far by this thread has completed (warp-collective,
-// one elected lane issues).
-__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-        : "memory");
-}
 
 // 32 lanes x 32 bits, 16 or 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
