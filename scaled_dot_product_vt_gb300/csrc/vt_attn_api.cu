@@ -426,6 +426,12 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
             if (merge_bytes > static_cast<long long>(p.stages) * stage_bytes) cl = 1;
         }
         p.cluster = cl;
+        // Without a cluster or shares the ring needs no more stages than the key tiles plus the Q tiles take
+        // (a problem of a few key tiles then asks for far less shared memory).
+        if (cl == 1 && n_split == 1) {
+            const long long need = (S_k + f2::kBN - 1) / f2::kBN + q_stages(T);
+            if (need < p.stages) p.stages = static_cast<int>(need < 2 ? 2 : need);
+        }
         const long long ctas = units * (cl > 1 ? cl : n_split);
         if (ctas > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         p.n_units = static_cast<int>(units);
