@@ -205,7 +205,8 @@ __device__ __forceinline__ bool next_unit(Ctl &ctl, int n, Unit *out, const Attn
 // KQ: MMA K-steps (16 bf16 each) of Q K^T, D_qk rounded up: 2, 4, 6 or 8.
 // RING: value widths up to 64, where TMEM holds a three-slot score ring per query tile (below), so the next
 // key tile's scores are computed while the softmax works on the current ones.
-template <int KQ, bool RING>
+// SPLIT: the units are key-range shares whose partial results a merge kernel combines (split-KV).
+template <int KQ, bool RING, bool SPLIT>
 __global__ void __launch_bounds__(q2::kThreads, 1)
     attn_fwd_bf16_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -738,7 +739,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
             }
             const bool row_ok = q_row < p.S_q;
-            if (ok && p.n_split == 1) {
+            if (ok && !SPLIT) {
                 // ------------------------------------------------------------ epilogue: O = O_t / l
                 // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
                 if (n_my > 0) tc_fence_after();
@@ -777,7 +778,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
                 if (p.lse && row_ok)
                     p.lse[(static_cast<long long>(U.b) * p.H + U.h) * p.S_q + q_row] = lse_from(m_used, l);
-            } else if (ok && p.n_split > 1) {
+            } else if (ok && SPLIT) {
                 // ------------------------------------------------------------ epilogue: partial O, m, l
                 // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
                 // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
