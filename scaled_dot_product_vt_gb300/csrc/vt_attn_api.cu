@@ -385,19 +385,24 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
         // value widths up to 64 leave TMEM room for the score ring (S of the next key tile during the softmax)
         const bool ring = p.n_pv <= 64;
-        // kernel variants: K-steps of Q K^T, the score ring, and partial outputs for a split-KV merge
+        // kernel variants: K-steps of Q K^T, the score ring, partial outputs for a split-KV merge, and a positive
+        // scale folded into the exponent
         using Kern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams);
-        auto pick = [&](auto ring_c, auto split_c) -> Kern {
-            constexpr bool R = decltype(ring_c)::value, S = decltype(split_c)::value;
-            return ksteps <= 2   ? attn_fwd_bf16_2q_kernel<2, R, S>
-                   : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, R, S>
-                   : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, R, S>
-                                 : attn_fwd_bf16_2q_kernel<8, R, S>;
+        auto pick = [&](auto ring_c, auto split_c, auto fold_c) -> Kern {
+            constexpr bool R = decltype(ring_c)::value, S = decltype(split_c)::value, F = decltype(fold_c)::value;
+            return ksteps <= 2   ? attn_fwd_bf16_2q_kernel<2, R, S, F>
+                   : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, R, S, F>
+                   : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, R, S, F>
+                                 : attn_fwd_bf16_2q_kernel<8, R, S, F>;
         };
-        using T_ = std::true_type;
-        using F_ = std::false_type;
-        const bool split = n_split > 1;
-        const Kern kern = ring ? (split ? pick(T_{}, T_{}) : pick(T_{}, F_{})) : (split ? pick(F_{}, T_{}) : pick(F_{}, F_{}));
+        auto pick_rs = [&](auto fold_c) -> Kern {
+            using T_ = std::true_type;
+            using F_ = std::false_type;
+            const bool split = n_split > 1;
+            return ring ? (split ? pick(T_{}, T_{}, fold_c) : pick(T_{}, F_{}, fold_c))
+                        : (split ? pick(F_{}, T_{}, fold_c) : pick(F_{}, F_{}, fold_c));
+        };
+        const Kern kern = p.scale_log2 > 0.0f ? pick_rs(std::true_type{}) : pick_rs(std::false_type{});
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<grid, q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;

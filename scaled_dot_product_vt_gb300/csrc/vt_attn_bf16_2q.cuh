@@ -206,7 +206,8 @@ __device__ __forceinline__ bool next_unit(Ctl &ctl, int n, Unit *out, const Attn
 // RING: value widths up to 64, where TMEM holds a three-slot score ring per query tile (below), so the next
 // key tile's scores are computed while the softmax works on the current ones.
 // SPLIT: the units are key-range shares whose partial results a merge kernel combines (split-KV).
-template <int KQ, bool RING, bool SPLIT>
+// FOLD: the scale is positive and folds into the exponent; otherwise the scores are scaled first.
+template <int KQ, bool RING, bool SPLIT, bool FOLD>
 __global__ void __launch_bounds__(q2::kThreads, 1)
     attn_fwd_bf16_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -587,9 +588,8 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
         // score ring: slots from column 192 t, O_t at 384 + 64 t (see the MMA issuer); otherwise S_t and O_t
         const uint32_t s_base = tmem + lane_base + (RING ? static_cast<uint32_t>(t * 192) : col_s(t));
         const uint32_t o_addr = tmem + lane_base + (RING ? static_cast<uint32_t>(384 + t * 64) : col_o(t));
-        // Non-positive scales are applied to the scores first, so the folded form below sees c > 0.
-        const bool fold = p.scale_log2 > 0.0f;
-        const float c = fold ? p.scale_log2 : 1.0f;
+        // Non-positive scales are applied to the scores first (FOLD false), so the folded form below sees c > 0.
+        const float c = FOLD ? p.scale_log2 : 1.0f;
         const float2 c2 = make_float2(c, c);
         uint32_t s_par = 0, o_par = 0;  // parities of the next scores and the next o_done of this tile
         uint32_t g = 0;                 // score ring: scores of this tile seen over the CTA's life
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 float s[BN];
                 #pragma unroll
                 for (int k = 0; k < BN; ++k) s[k] = __uint_as_float(sr[k]);
-                if (!fold) {
+                if constexpr (!FOLD) {
                     #pragma unroll
                     for (int k = 0; k < BN; ++k) s[k] *= p.scale_log2;
                 }
