@@ -446,10 +446,16 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         if (ctas > 0x7FFFFFFFll) return VT_ERR_UNSUPPORTED;
         p.n_units = static_cast<int>(units);
         const int smem = 1024 + p.stages * stage_bytes;
-        void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams) =
-            dq <= 32 ? attn_fwd_f32_2q_kernel<4>
-                     : dq <= 64 ? attn_fwd_f32_2q_kernel<8>
-                                : dq <= 96 ? attn_fwd_f32_2q_kernel<12> : attn_fwd_f32_2q_kernel<16>;
+        // Q K^T K-steps, and a positive scale folded into the exponent (a variant without the scores' scaling)
+        using Kern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams);
+        auto pick = [&](auto fold_c) -> Kern {
+            constexpr bool F = decltype(fold_c)::value;
+            return dq <= 32   ? attn_fwd_f32_2q_kernel<4, F>
+                   : dq <= 64 ? attn_fwd_f32_2q_kernel<8, F>
+                   : dq <= 96 ? attn_fwd_f32_2q_kernel<12, F>
+                              : attn_fwd_f32_2q_kernel<16, F>;
+        };
+        const Kern kern = p.scale_log2 > 0.0f ? pick(std::true_type{}) : pick(std::false_type{});
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);

@@ -132,7 +132,7 @@ __device__ __forceinline__ bool unit_valid(const AttnParams &p, const Unit &U) {
 
 // KQ: the most MMA K-steps (8 tf32 each) of Q K^T the instantiation runs (D_qk rounded up to 8, then to
 // 32, 64, 96 or 128); the steps past D_qk are skipped.
-template <int KQ>
+template <int KQ, bool FOLD>
 __global__ void __launch_bounds__(f2::kThreads, 1)
     attn_fwd_f32_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -464,9 +464,8 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
         }
         const uint32_t s_addr = tmem + lane_base + col_s0 + t * BN;
         const uint32_t o_addr = tmem + lane_base + col_o0 + t * p.n_pv;
-        // Non-positive scales are applied to the scores first, so the folded form below sees c > 0.
-        const bool fold = p.scale_log2 > 0.0f;
-        const float c = fold ? p.scale_log2 : 1.0f;
+        // Non-positive scales are applied to the scores first (FOLD false), so the folded form below sees c > 0.
+        const float c = FOLD ? p.scale_log2 : 1.0f;
         const float2 c2 = make_float2(c, c);
         const int key_lo = band_key_lo(p, q_row), key_hi = band_key_hi(p, q_row);
         const int tile_row0 = U.r0 + t * kBM;
@@ -486,7 +485,7 @@ __global__ void __launch_bounds__(f2::kThreads, 1)
             float x[BN];
 #pragma unroll
             for (int k = 0; k < BN; ++k) x[k] = __uint_as_float(sr[k]);
-            if (!fold) {
+            if constexpr (!FOLD) {
 #pragma unroll
                 for (int k = 0; k < BN; ++k) x[k] *= p.scale_log2;
             }
