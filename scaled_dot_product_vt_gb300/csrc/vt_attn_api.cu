@@ -385,24 +385,37 @@ vt_status launch(const Problem &P, const vt_attn_opts *opts, int n_split, void *
         const int ksteps = static_cast<int>((D_qk + 15) / 16);
         // value widths up to 64 leave TMEM room for the score ring (S of the next key tile during the softmax)
         const bool ring = p.n_pv <= 64;
-        // kernel variants: K-steps of Q K^T, the score ring, partial outputs for a split-KV merge, and a positive
+        // kernel variants: K-steps of Q K^T, the score ring, the epilogue (O in any layout with the log-sum-exp;
+        // partial outputs for a split-KV merge; O alone in 32-byte rows of whole 16-column groups), and a positive
         // scale folded into the exponent
         using Kern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const AttnParams);
-        auto pick = [&](auto ring_c, auto split_c, auto fold_c) -> Kern {
-            constexpr bool R = decltype(ring_c)::value, S = decltype(split_c)::value, F = decltype(fold_c)::value;
-            return ksteps <= 2   ? attn_fwd_bf16_2q_kernel<2, R, S, F>
-                   : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, R, S, F>
-                   : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, R, S, F>
-                                 : attn_fwd_bf16_2q_kernel<8, R, S, F>;
+        auto pick = [&](auto ring_c, auto epi_c, auto fold_c) -> Kern {
+            constexpr bool R = decltype(ring_c)::value, F = decltype(fold_c)::value;
+            constexpr int E = decltype(epi_c)::value;
+            return ksteps <= 2   ? attn_fwd_bf16_2q_kernel<2, R, E, F>
+                   : ksteps <= 4 ? attn_fwd_bf16_2q_kernel<4, R, E, F>
+                   : ksteps <= 6 ? attn_fwd_bf16_2q_kernel<6, R, E, F>
+                                 : attn_fwd_bf16_2q_kernel<8, R, E, F>;
         };
-        auto pick_rs = [&](auto fold_c) -> Kern {
-            using T_ = std::true_type;
-            using F_ = std::false_type;
-            const bool split = n_split > 1;
-            return ring ? (split ? pick(T_{}, T_{}, fold_c) : pick(T_{}, F_{}, fold_c))
-                        : (split ? pick(F_{}, T_{}, fold_c) : pick(F_{}, F_{}, fold_c));
-        };
-        const Kern kern = p.scale_log2 > 0.0f ? pick_rs(std::true_type{}) : pick_rs(std::false_type{});
+        using T_ = std::true_type;
+        using F_ = std::false_type;
+        using Plain = std::integral_constant<int, q2::kEpiPlain>;
+        using Split = std::integral_constant<int, q2::kEpiSplit>;
+        using Fast = std::integral_constant<int, q2::kEpiPlainFast>;
+        const bool fold = p.scale_log2 > 0.0f;
+        // (the short epilogue measured faster in the two-tile kernel and slower with the score ring)
+        const int epi = n_split > 1 ? q2::kEpiSplit
+                        : (fold && !ring && p.o_vec32 && D_v % 16 == 0 && !P.lse) ? q2::kEpiPlainFast
+                                                                                : q2::kEpiPlain;
+        Kern kern;
+        if (fold) {
+            kern = epi == q2::kEpiSplit       ? (ring ? pick(T_{}, Split{}, T_{}) : pick(F_{}, Split{}, T_{}))
+                   : epi == q2::kEpiPlainFast ? pick(F_{}, Fast{}, T_{})
+                                              : (ring ? pick(T_{}, Plain{}, T_{}) : pick(F_{}, Plain{}, T_{}));
+        } else {
+            kern = epi == q2::kEpiSplit ? (ring ? pick(T_{}, Split{}, F_{}) : pick(F_{}, Split{}, F_{}))
+                                        : (ring ? pick(T_{}, Plain{}, F_{}) : pick(F_{}, Plain{}, F_{}));
+        }
         if (!ensure_smem(reinterpret_cast<const void *>(kern), dev, smem)) return VT_ERR_CUDA;
         kern<<<grid, q2::kThreads, smem, stream>>>(tq, tk, tv, p);
         if (cudaGetLastError() != cudaSuccess) return VT_ERR_CUDA;

@@ -61,6 +61,7 @@ constexpr int kRegsControl = 72;    // warpgroup 0 after setmaxnreg
 constexpr int kRegsSoftmax = 216;   // softmax warpgroups after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch");
 constexpr int kMaxSlots = 6;
+constexpr int kEpiPlain = 0, kEpiSplit = 1, kEpiPlainFast = 2;  // epilogue variants (the kernel's EPI)
 constexpr int kUnitRing = 4;        // unit indices in flight between the producer and the other roles
 constexpr int kUnitReaders = 1 + 8;  // the MMA warp and one lane of each softmax warp (one more MMA warp with the score ring)
 constexpr uint32_t kTmemCols = 512;
@@ -205,9 +206,11 @@ __device__ __forceinline__ bool next_unit(Ctl &ctl, int n, Unit *out, const Attn
 // KQ: MMA K-steps (16 bf16 each) of Q K^T, D_qk rounded up: 2, 4, 6 or 8.
 // RING: value widths up to 64, where TMEM holds a three-slot score ring per query tile (below), so the next
 // key tile's scores are computed while the softmax works on the current ones.
-// SPLIT: the units are key-range shares whose partial results a merge kernel combines (split-KV).
+// EPI: what the epilogue writes.  kEpiPlain: O (any alignment, any D_v, the log-sum-exp if asked for);
+// kEpiSplit: the partial results of a key-range share, for the split-KV merge kernel; kEpiPlainFast: O only,
+// 32-byte aligned rows and D_v a multiple of 16 (the common case, with no other store forms in the code).
 // FOLD: the scale is positive and folds into the exponent; otherwise the scores are scaled first.
-template <int KQ, bool RING, bool SPLIT, bool FOLD>
+template <int KQ, bool RING, int EPI, bool FOLD>
 __global__ void __launch_bounds__(q2::kThreads, 1)
     attn_fwd_bf16_2q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -739,7 +742,7 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                 }
             }
             const bool row_ok = q_row < p.S_q;
-            if (ok && !SPLIT) {
+            if (ok && EPI != kEpiSplit) {
                 // ------------------------------------------------------------ epilogue: O = O_t / l
                 // A row with no allowed key (l = 0, or no key tile at all) is written as 0.
                 if (n_my > 0) tc_fence_after();
@@ -761,7 +764,9 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                     #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         w[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-                    if (cc + 16 <= p.D_v) {
+                    if constexpr (EPI == kEpiPlainFast) {
+                        st_global_v8(orow + cc * 2, w);  // one 32-byte store per 16 columns
+                    } else if (cc + 16 <= p.D_v) {
                         if (p.o_vec32) {  // half as many store instructions, each a full 32-byte sector
                             st_global_v8(orow + cc * 2, w);
                         } else {
@@ -776,9 +781,9 @@ __global__ void __launch_bounds__(q2::kThreads, 1)
                             if (cc + k < p.D_v) dst[k] = static_cast<uint16_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
                     }
                 }
-                if (p.lse && row_ok)
+                if (EPI == kEpiPlain && p.lse && row_ok)
                     p.lse[(static_cast<long long>(U.b) * p.H + U.h) * p.S_q + q_row] = lse_from(m_used, l);
-            } else if (ok && SPLIT) {
+            } else if (ok && EPI == kEpiSplit) {
                 // ------------------------------------------------------------ epilogue: partial O, m, l
                 // Unnormalised O_t with its reference max m (log2 units) and sum l; a share with no
                 // key tile for this query tile writes the empty partial (m = -inf, l = 0, O = 0).
