@@ -36,23 +36,46 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerBlock)
     const int lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * kMergeRowsPerBlock + (threadIdx.x >> 5);
     if (row >= mp.rows) return;
+    // One pass over the shares in groups of four: a group's m, l, correction and O values are all loaded
+    // before any is used (one memory round trip per group), and the running sums are rescaled when the
+    // running max M grows:  M' = max(M, m_s),  sums *= 2^(M - M'),  then each share adds 2^(m_s - M') times its own.
     float M = -INFINITY;
-    for (int s = 0; s < mp.n_split; ++s) M = fmaxf(M, mp.part_m[s * mp.rows + row]);
     float L = 0.0f;   // sum of the shares' l: the log-sum-exp
     float Lo = 0.0f;  // sum of l + corr: the divisor of O, weighing P as P V used it
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < mp.n_split; ++s) {
-        const float ms = mp.part_m[s * mp.rows + row];
-        if (ms == -INFINITY) continue;  // no allowed key in this share
-        const float w = ex2(ms - M);
-        L += w * mp.part_l[s * mp.rows + row];
-        Lo += w * (mp.part_l[s * mp.rows + row] + mp.part_c[s * mp.rows + row]);
-        const float *po = mp.part_o + (s * mp.rows + row) * mp.D_v;
+    for (int s0 = 0; s0 < mp.n_split; s0 += 4) {
+        float ms[4], ls[4], cs[4], o[4][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int col = lane + 32 * c;
-            if (col < mp.D_v) acc[c] += w * po[col];
+        for (int u = 0; u < 4; ++u) {
+            const bool in = s0 + u < mp.n_split;
+            const long long idx = static_cast<long long>(s0 + u) * mp.rows + row;
+            ms[u] = in ? mp.part_m[idx] : -INFINITY;
+            ls[u] = in ? mp.part_l[idx] : 0.0f;
+            cs[u] = in ? mp.part_c[idx] : 0.0f;
+            const float *po = mp.part_o + idx * mp.D_v;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col = lane + 32 * c;
+                o[u][c] = (in && col < mp.D_v) ? po[col] : 0.0f;
+            }
         }
+        const float Mn = fmaxf(fmaxf(M, fmaxf(ms[0], ms[1])), fmaxf(ms[2], ms[3]));
+        if (Mn == -INFINITY) continue;  // no allowed key in any share so far
+        const float r = M == -INFINITY ? 0.0f : ex2(M - Mn);
+        L *= r;
+        Lo *= r;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] *= r;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (ms[u] == -INFINITY) continue;  // no allowed key in this share (or no share)
+            const float w = ex2(ms[u] - Mn);
+            L += w * ls[u];
+            Lo += w * (ls[u] + cs[u]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[c] += w * o[u][c];
+        }
+        M = Mn;
     }
     const float inv = L > 0.0f ? 1.0f / Lo : 0.0f;  // no share saw an allowed key: the row is 0
     if (mp.lse && lane == 0) mp.lse[row] = lse_from(M, L);
