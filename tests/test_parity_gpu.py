@@ -126,10 +126,13 @@ def test_edge_f32(shape):
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.3, 2.5])
-def test_unusual_scales(scale):
-    q, k, v = synth.make_qkv(1, 2, 150, 140, 64, 64, "bf16", seed=11)
+@pytest.mark.parametrize("D", [64, 128])
+def test_unusual_scales(scale, D):
+    """Zero and negative scales take the kernel variants that scale the scores before the exponent;
+    D = 64 runs the score-ring kernel, D = 128 the two-tile kernel."""
+    q, k, v = synth.make_qkv(1, 2, 150, 140, D, D, "bf16", seed=11)
     for causal in (False, True):
-        check(run(q, k, v, scale, causal), oracle.attn_fwd(q, k, v, scale, causal), "bf16", f"scale={scale}")
+        check(run(q, k, v, scale, causal), oracle.attn_fwd(q, k, v, scale, causal), "bf16", f"scale={scale} D={D}")
 
 
 def _tf32_exact(x: np.ndarray) -> np.ndarray:

@@ -50,6 +50,19 @@ def test_splitkv_matches_oracle(case):
     assert np.abs(got - plain).max() <= 2e-2
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("scale", [-0.2, 0.0])
+def test_splitkv_non_positive_scale(dtype, scale):
+    """Split-KV shares with a scale that cannot fold into the exponent (the partial-output and merge path of
+    the kernel variants that scale the scores first)."""
+    B, H, S_q, S_k, D = 1, 2, 300, 1500, (128 if dtype == "bf16" else 72)
+    q, k, v = synth.make_qkv(B, H, S_q, S_k, D, D, dtype, seed=29)
+    Q, K, V = to_device(q), to_device(k), to_device(v)
+    got = to_host64(vt.attn_fwd_splitkv(Q, K, V, scale=scale, causal=True, n_split=3))
+    assert vt.vt_last_device_status() == 0
+    check(got, oracle.attn_fwd(q, k, v, scale, True), dtype, f"split-KV scale={scale}")
+
+
 CASES_F32 = [
     # B, H, S_q, S_k, D_qk, D_v, causal, n_split (fp32 I/O, TF32 path; 64-key tiles)
     (2, 4, 1000, 1000, 72, 72, True, 2),    # the mid fp32 workload's shape
