@@ -5,7 +5,7 @@
 // real arithmetic O[r] = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s for any M; M = max_s m_s
 // keeps every weight <= 1.  This is the continuation step of the coverage table's
 // attention_fwd_triton3 row (case 4 reads M, L and Out and merges a further key range), applied
-// to all shares at once.  HBM-bound: per row it reads n_split * (D_v + 2) floats and writes D_v.
+// to all shares at once.  HBM-bound: per row it reads n_split * (D_v + 3) floats (O, m, l and the correction) and writes D_v.
 // The row's log-sum-exp, if asked for, is M + log2(L) in natural-log units.
 #pragma once
 
