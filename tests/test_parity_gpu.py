@@ -182,13 +182,15 @@ SENT32 = 0x7FC0DEAD
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shift", [0, 16])
-def test_write_set_guard_bands(dtype, causal, shift):
+@pytest.mark.parametrize("D_v", [24, 128])
+def test_write_set_guard_bands(dtype, causal, shift, D_v):
     """Only O[b,h,i<S_q,e<D_v] is written: padding columns, padding rows and 4 KiB canaries stay bit-exact.
-    shift = 16 starts O 16 bytes past a 32-byte boundary (the bf16 epilogue then stores 16 bytes at a time)."""
-    B, H, S_q, S_k, D_qk, D_v = 2, 3, 201, 150, 40, 24
+    shift = 16 starts O 16 bytes past a 32-byte boundary (the bf16 epilogue then stores 16 bytes at a time);
+    D_v = 128 with shift 0 takes the bf16 two-tile kernel's short epilogue (32-byte rows, whole 16-column groups)."""
+    B, H, S_q, S_k, D_qk = 2, 3, 201, 150, 40
     q, k, v = synth.make_qkv(B, H, S_q, S_k, D_qk, D_v, dtype, seed=14)
     elt = 2 if dtype == "bf16" else 4
-    pad_d, pad_s = 8, 3
+    pad_d, pad_s = (8 if D_v == 24 else 32), 3
     row = D_v + pad_d
     o_strides = (H * (S_q + pad_s) * row, (S_q + pad_s) * row, row)
     canary = 4096 // elt
